@@ -1,0 +1,320 @@
+#!/usr/bin/env python3
+"""Benchmark: q8 verify attention over an FP8 E4M3 paged KV cache at 262144
+tokens of context (the long-context workload), on GB300.
+
+One step = one verify call (split kernel + combine kernel) over the whole
+workload: B=1, q=8, 6 q heads on 1 KV head, D=256, L=262144, 16-token pages.
+`value` is the KV-read bandwidth of the whole job (algorithmic K+V bytes,
+1 byte per element, / time), summed over ranks; `us_per_step` is the latency.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas, one per GPU (the operation does not shard
+across GPUs: there is no exchange step); launch it with torchrun.  The
+`--impl reference` arm times the FP64 CPU oracle on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per q8 verify step and KV-read GB/s (% of HBM peak) at 262144 ctx"
+WORKLOAD = "long"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_desc(w):
+    s = w.spec
+    return (f"{s.name}: B{s.B} q{int(w.q_len[0])} Hq{s.Hq} Hkv{s.Hkv} D{s.D} "
+            f"L{int(w.seq_len.max())} page{s.page}" + (" outliers" if s.outliers else ""))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic():
+    """DRAM bytes per launch of the split kernel from a committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "split_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    h = hashlib.sha256(open(os.path.join(ROOT, d["source"]), "rb").read()).hexdigest()
+    if d.get("source_sha256") != h:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.proc = None
+        self.uuid = uuid
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_step(w, rows, threads=0):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.verify_attn(w.q, w.kv_pages, w.block_table, w.seq_len, w.q_len, w.kv_scales,
+                       sm_scale=w.sm_scale, rows=rows, threads=threads)
+    return time.perf_counter() - t0
+
+
+def all_rows(w):
+    return np.array([(b, i, hq) for b in range(w.spec.B) for i in range(int(w.q_len[b]))
+                     for hq in range(w.spec.Hq)], dtype=np.int32)
+
+
+def run_reference(args, w):
+    """The FP64 CPU oracle, timed on the host cores: each step evaluates a
+    bounded sample of the workload's output rows; the rate is scaled to the
+    whole step."""
+    import oracle
+    rows = all_rows(w)
+    n = min(len(rows), 12)
+    threads = oracle.max_threads()
+    k = 0
+    for _ in range(args.warmup):
+        cpu_oracle_step(w, rows[[(k + j) % len(rows) for j in range(n)]])
+        k += n
+    times = []
+    for _ in range(args.steps):
+        times.append(cpu_oracle_step(w, rows[[(k + j) % len(rows) for j in range(n)]]))
+        k += n
+    per_step = sum(times) / len(times) * len(rows) / n  # seconds for all rows
+    gbs = w.kv_bytes / per_step / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "us_per_step": per_step * 1e6, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w)},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of {len(rows)} output rows per step, scaled to all"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    import workloads as W
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        run_reference(args, W.generate(args.workload))
+        return 0
+
+    import torch
+    import fp8_paged_attention_e4m3_gb300 as vae4
+
+    assert torch.cuda.is_available(), "bench needs a GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    vae4.load()
+
+    w = W.generate(args.workload)
+    s = w.spec
+    q, kv, bt, seq, sc = W.to_device(w, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    pool_bytes = kv.numel()
+    R = max(2, math.ceil(3 * l2 / pool_bytes))
+    kvs = [kv] + [kv.clone() for _ in range(R - 1)]  # same bytes, other addresses
+    out = torch.zeros_like(q)
+    T = s.partition_tokens
+    T_eff, P = vae4.plan(s.B, s.Hkv, w.capacity, T)
+    ws = vae4.alloc_workspace(s.B, s.Hq, s.Hkv, s.Qmax, s.D, w.capacity, T, device=dev)
+    kw = dict(partition_tokens=T, max_seq_len=w.capacity)
+
+    for k in range(max(3, args.warmup)):
+        vae4.verify(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
+    torch.cuda.synchronize()
+    assert vae4.read_status(ws) == 0
+
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid else None)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        a, b = ev[k]
+        a.record(stream)
+        vae4.verify_attn_e4m3_partials(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
+        b.record(stream)
+        vae4.verify_attn_e4m3_combine(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    split_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    assert vae4.read_status(ws) == 0
+    gpu_launches = 2 * args.steps
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    h_in = [torch.from_numpy(w.q).pin_memory(), torch.from_numpy(w.kv_pages).pin_memory(),
+            torch.from_numpy(w.block_table).pin_memory(), seq.cpu().pin_memory(),
+            torch.from_numpy(w.kv_scales).pin_memory()]
+    h_out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    d_in = [q, kvs[0], bt, seq, sc]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        vae4.verify(d_in[0], d_in[1], d_in[2], d_in[3], d_in[4], out, ws, **kw)
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    t_step = total_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_step, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, e2e_ms = float(t[0]), float(t[1])
+    kv_bytes = w.kv_bytes
+    value = world * kv_bytes / (t_step * 1e-3) / 1e9
+    e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
+
+    if rank == 0:
+        peak, peak_kind = peaks()
+        split_mean = statistics.mean(split_us)
+        achieved = kv_bytes / (split_mean * 1e-6) / 1e9
+        traffic = kernel_traffic()
+        rows = all_rows(w)
+        n_cpu = len(rows)
+        cpu_s = cpu_oracle_step(w, rows)
+        import oracle
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s",
+            "us_per_step": t_step * 1e3, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "precision": {"kv": "e4m3", "operands": "f16", "state": "f32", "out": "f16"},
+            "data": "synthetic",
+            "config": {"workload": workload_desc(w), "seed": s.seed,
+                       "partition_tokens": T_eff, "partitions": P,
+                       "l2": f"inputs rotate over {R} KV pool copies of {pool_bytes >> 20} MiB "
+                             f"(> 3x the {l2 >> 20} MiB L2)"},
+            "pct_of_hbm_peak": 100.0 * value / world / peak,
+            "roofline": {"bound": "hbm", "kernel": "split (partials)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                         "traffic": traffic,
+                         "split_us_mean": split_mean, "split_us_median": statistics.median(split_us)},
+            "cpu_baseline": {"value": kv_bytes / cpu_s / 1e9, "unit": "GB/s",
+                             "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"one full step: all {n_cpu} output rows, FP64",
+                             "seconds": cpu_s},
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": gpu_launches,
+            "clocks": clocks,
+            "gpu": props.name,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,390 @@
+// C-ABI entry points: argument validation, the split-K partition plan, the
+// workspace layout and the kernel launches.  See include/verify_attn_e4m3.h
+// for the contract of every function.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "kernels.h"
+#include "params.h"
+#include "verify_attn_e4m3.h"
+
+namespace {
+
+using vae4::CombineParams;
+using vae4::SplitParams;
+
+constexpr int64_t kStatusBytes = 256;  // status word + padding
+constexpr int kMaxRowsPad = 96;        // Qmax * G rounded to 16 (q16 x GQA6)
+constexpr int kMaxQmax = 16;
+constexpr int64_t kMaxPartitions = 8192;  // per (sequence, KV head)
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  int64_t ml_off, o_off, total;
+};
+
+WsLayout ws_layout(int B, int Hkv, int P, int rows_pad, int D) {
+  WsLayout l;
+  l.ml_off = kStatusBytes;
+  const int64_t ml_bytes = (int64_t)B * Hkv * P * rows_pad * 2 * 4;
+  l.o_off = align_up(l.ml_off + ml_bytes, 256);
+  l.total = l.o_off + (int64_t)B * Hkv * P * rows_pad * D * 4;
+  return l;
+}
+
+int do_plan(int B, int Hkv, int cap, int T_req, int num_sms, int *T_out, int *P_out) {
+  if (B < 1 || Hkv < 1 || cap < 1 || num_sms < 1) return VAE4_ERR_SHAPE;
+  int64_t T;
+  if (T_req < 0 || (T_req > 0 && T_req % 16 != 0)) return VAE4_ERR_PARTITION;
+  if (T_req > 0) {
+    T = T_req;
+  } else {
+    const int64_t units = (int64_t)B * Hkv;
+    const int64_t pmax = std::max<int64_t>(1, num_sms / units);
+    T = align_up((cap + pmax - 1) / pmax, 16);
+    T = std::max<int64_t>(T, 64);
+  }
+  const int64_t P = (cap + T - 1) / T;
+  if (P > kMaxPartitions) return VAE4_ERR_PARTITION;
+  *T_out = (int)T;
+  *P_out = (int)P;
+  return VAE4_OK;
+}
+
+int device_sms(int *out) {
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VAE4_ERR_CUDA;
+  if (dev >= 0 && dev < 128 && cache[dev] > 0) {
+    *out = cache[dev];
+    return VAE4_OK;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return VAE4_ERR_CUDA;
+  if (dev >= 0 && dev < 128) cache[dev] = n;
+  *out = n;
+  return VAE4_OK;
+}
+
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// q / out: F16 [B][Qmax][Hq][D], stride[3] == 1, other strides multiples of 8.
+int check_qo(const vae4_tensor *t) {
+  if (t->dtype != VAE4_F16) return VAE4_ERR_DTYPE;
+  if (t->ndim != 4) return VAE4_ERR_SHAPE;
+  for (int k = 0; k < 4; ++k)
+    if (t->shape[k] < 0) return VAE4_ERR_SHAPE;
+  if (t->stride[3] != 1) return VAE4_ERR_STRIDE;
+  for (int k = 0; k < 3; ++k)
+    if (t->stride[k] % 8 != 0 || t->stride[k] < 0) return VAE4_ERR_STRIDE;
+  if (!al16(t->data)) return VAE4_ERR_MISALIGNED;
+  return VAE4_OK;
+}
+
+struct Prepared {
+  SplitParams sp;
+  CombineParams cp;
+  int64_t ws_needed;
+  bool empty;
+};
+
+int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
+            const vae4_tensor *seq, const vae4_tensor *sc, const vae4_tensor *out,
+            const vae4_tensor *ws, const vae4_options *opt, Prepared *pr) {
+  if (!q || !kv || !bt || !seq || !sc || !out || !ws) return VAE4_ERR_NULL;
+  vae4_options o;
+  memset(&o, 0, sizeof(o));
+  if (opt) o = *opt;
+  if (o.flags != 0) return VAE4_ERR_OPTIONS;
+
+  int rc = check_qo(q);
+  if (rc) return rc;
+  rc = check_qo(out);
+  if (rc) return rc;
+  for (int k = 0; k < 4; ++k)
+    if (out->shape[k] != q->shape[k]) return VAE4_ERR_SHAPE;
+  const int64_t B = q->shape[0], Qmax = q->shape[1], Hq = q->shape[2], D = q->shape[3];
+  if (D != 64 && D != 128 && D != 256) return VAE4_ERR_UNSUPPORTED;
+  if (Qmax < 1 || Qmax > kMaxQmax || Hq < 1 || B > 65535) return VAE4_ERR_SHAPE;
+
+  // kv pages: U8 [n_pages][2][Hkv][page][D], contiguous
+  if (kv->dtype != VAE4_U8) return VAE4_ERR_DTYPE;
+  if (kv->ndim != 5 || kv->shape[1] != 2 || kv->shape[4] != D || kv->shape[0] < 1 ||
+      kv->shape[2] < 1)
+    return VAE4_ERR_SHAPE;
+  const int64_t n_pages = kv->shape[0], Hkv = kv->shape[2], page = kv->shape[3];
+  if (page != 16 && page != 32 && page != 64 && page != 128) return VAE4_ERR_UNSUPPORTED;
+  if (kv->stride[4] != 1 || kv->stride[3] != D || kv->stride[2] != page * D ||
+      kv->stride[1] != Hkv * page * D || kv->stride[0] != 2 * Hkv * page * D)
+    return VAE4_ERR_STRIDE;
+  if (!al16(kv->data)) return VAE4_ERR_MISALIGNED;
+  if (Hq % Hkv != 0) return VAE4_ERR_GQA;
+  const int64_t G = Hq / Hkv;
+  const int64_t rows = Qmax * G;
+  const int64_t rows_pad = align_up(rows, 16);
+  if (rows_pad > kMaxRowsPad) return VAE4_ERR_UNSUPPORTED;
+
+  // block table: I32 [B][max_pages]
+  if (bt->dtype != VAE4_I32) return VAE4_ERR_DTYPE;
+  if (bt->ndim != 2 || bt->shape[0] != B || bt->shape[1] < 1) return VAE4_ERR_SHAPE;
+  if (bt->stride[1] != 1 || bt->stride[0] < 0) return VAE4_ERR_STRIDE;
+  const int64_t max_pages = bt->shape[1];
+
+  // lengths: I32 [B] or [B][2]
+  if (seq->dtype != VAE4_I32) return VAE4_ERR_DTYPE;
+  int has_qlen = 0;
+  if (seq->ndim == 1) {
+    if (seq->shape[0] != B) return VAE4_ERR_SHAPE;
+  } else if (seq->ndim == 2) {
+    if (seq->shape[0] != B || seq->shape[1] != 2) return VAE4_ERR_SHAPE;
+    if (seq->stride[1] != 1) return VAE4_ERR_STRIDE;
+    has_qlen = 1;
+  } else {
+    return VAE4_ERR_SHAPE;
+  }
+  if (seq->stride[0] < 0 || seq->stride[0] > INT32_MAX) return VAE4_ERR_STRIDE;
+
+  // scales: F32 [Hkv][2]
+  if (sc->dtype != VAE4_F32) return VAE4_ERR_DTYPE;
+  if (sc->ndim != 2 || sc->shape[0] != Hkv || sc->shape[1] != 2) return VAE4_ERR_SHAPE;
+  if (sc->stride[1] != 1 || sc->stride[0] < 0 || sc->stride[0] > INT32_MAX) return VAE4_ERR_STRIDE;
+
+  // workspace: U8 [bytes], 256-byte aligned
+  if (ws->dtype != VAE4_U8) return VAE4_ERR_DTYPE;
+  if (ws->ndim != 1 || ws->stride[0] != 1) return VAE4_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(ws->data) & 255u) != 0) return VAE4_ERR_WORKSPACE;
+
+  const int64_t table_cap = max_pages * page;
+  int64_t cap = o.max_seq_len > 0 ? o.max_seq_len : table_cap;
+  if (o.max_seq_len < 0 || cap > table_cap || cap > INT32_MAX / 2) return VAE4_ERR_SHAPE;
+
+  int sms = o.num_sms;
+  if (sms < 0) return VAE4_ERR_SHAPE;
+  if (sms == 0 && B > 0) {
+    rc = device_sms(&sms);
+    if (rc) return rc;
+  }
+  int T = 0, P = 0;
+  if (B > 0) {
+    rc = do_plan((int)B, (int)Hkv, (int)cap, o.partition_tokens, sms, &T, &P);
+    if (rc) return rc;
+  }
+  const WsLayout lay = ws_layout((int)B, (int)Hkv, P, (int)rows_pad, (int)D);
+  pr->ws_needed = lay.total;
+  pr->empty = (B == 0);
+  if (B > 0 && ws->shape[0] < lay.total) return VAE4_ERR_WORKSPACE;
+  if (!q->data || !kv->data || !bt->data || !seq->data || !sc->data || !out->data ||
+      !ws->data) {
+    if (B > 0) return VAE4_ERR_NULL;
+  }
+
+  float sm_scale = o.softmax_scale;
+  if (!(sm_scale > 0.f)) {
+    if (sm_scale != 0.f) return VAE4_ERR_OPTIONS;
+    sm_scale = 1.0f / sqrtf((float)D);
+  }
+  uint8_t *wsb = static_cast<uint8_t *>(ws->data);
+
+  SplitParams &s = pr->sp;
+  memset(&s, 0, sizeof(s));
+  s.q = q->data;
+  s.q_sb = q->stride[0];
+  s.q_si = q->stride[1];
+  s.q_sh = q->stride[2];
+  s.kv = static_cast<const uint8_t *>(kv->data);
+  s.n_pages = n_pages;
+  s.bt = static_cast<const int32_t *>(bt->data);
+  s.bt_sb = bt->stride[0];
+  s.max_pages = (int32_t)max_pages;
+  s.seq = static_cast<const int32_t *>(seq->data);
+  s.seq_sb = (int32_t)seq->stride[0];
+  s.seq_has_qlen = has_qlen;
+  s.scales = static_cast<const float *>(sc->data);
+  s.scale_sh = (int32_t)sc->stride[0];
+  s.ws_ml = reinterpret_cast<float *>(wsb + lay.ml_off);
+  s.ws_o = reinterpret_cast<float *>(wsb + lay.o_off);
+  s.status = reinterpret_cast<uint32_t *>(wsb);
+  s.B = (int32_t)B;
+  s.Qmax = (int32_t)Qmax;
+  s.Hq = (int32_t)Hq;
+  s.Hkv = (int32_t)Hkv;
+  s.G = (int32_t)G;
+  s.D = (int32_t)D;
+  s.page = (int32_t)page;
+  s.rows = (int32_t)rows;
+  s.rows_pad = (int32_t)rows_pad;
+  s.T = T;
+  s.P = P;
+  s.capacity = (int32_t)cap;
+  s.sm_scale = sm_scale;
+
+  CombineParams &c = pr->cp;
+  memset(&c, 0, sizeof(c));
+  c.ws_ml = s.ws_ml;
+  c.ws_o = s.ws_o;
+  c.out = out->data;
+  c.o_sb = out->stride[0];
+  c.o_si = out->stride[1];
+  c.o_sh = out->stride[2];
+  c.seq = s.seq;
+  c.seq_sb = s.seq_sb;
+  c.seq_has_qlen = has_qlen;
+  c.scales = s.scales;
+  c.scale_sh = s.scale_sh;
+  c.B = s.B;
+  c.Qmax = s.Qmax;
+  c.Hq = s.Hq;
+  c.Hkv = s.Hkv;
+  c.G = s.G;
+  c.D = s.D;
+  c.rows_pad = s.rows_pad;
+  c.T = T;
+  c.P = P;
+  c.capacity = s.capacity;
+  return VAE4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int verify_attn_e4m3_ex(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                        const vae4_tensor *block_table, const vae4_tensor *seq_lens,
+                        const vae4_tensor *kv_scales, const vae4_tensor *out,
+                        const vae4_tensor *workspace, vae4_stream stream,
+                        const vae4_options *opt) {
+  Prepared pr;
+  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  if (rc) return rc;
+  if (pr.empty) return VAE4_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (vae4::launch_split_mma(pr.sp, st) != cudaSuccess) return VAE4_ERR_CUDA;
+  if (vae4::launch_combine(pr.cp, st) != cudaSuccess) return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+int verify_attn_e4m3_partials(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                              const vae4_tensor *block_table, const vae4_tensor *seq_lens,
+                              const vae4_tensor *kv_scales, const vae4_tensor *out,
+                              const vae4_tensor *workspace, vae4_stream stream,
+                              const vae4_options *opt) {
+  Prepared pr;
+  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  if (rc) return rc;
+  if (pr.empty) return VAE4_OK;
+  if (vae4::launch_split_mma(pr.sp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+int verify_attn_e4m3_combine(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                             const vae4_tensor *block_table, const vae4_tensor *seq_lens,
+                             const vae4_tensor *kv_scales, const vae4_tensor *out,
+                             const vae4_tensor *workspace, vae4_stream stream,
+                             const vae4_options *opt) {
+  Prepared pr;
+  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  if (rc) return rc;
+  if (pr.empty) return VAE4_OK;
+  if (vae4::launch_combine(pr.cp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+int verify_attn_e4m3(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                     const vae4_tensor *block_table, const vae4_tensor *seq_lens,
+                     const vae4_tensor *kv_scales, const vae4_tensor *out,
+                     const vae4_tensor *workspace, vae4_stream stream) {
+  return verify_attn_e4m3_ex(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace,
+                             stream, nullptr);
+}
+
+int verify_attn_e4m3_plan(int B, int Hkv, int max_seq_len, int partition_tokens, int num_sms,
+                          int32_t *partition_tokens_out, int32_t *partitions_out) {
+  if (!partition_tokens_out || !partitions_out) return VAE4_ERR_NULL;
+  int T = 0, P = 0;
+  const int rc = do_plan(B, Hkv, max_seq_len, partition_tokens, num_sms, &T, &P);
+  if (rc) return rc;
+  *partition_tokens_out = T;
+  *partitions_out = P;
+  return VAE4_OK;
+}
+
+int64_t verify_attn_e4m3_workspace_bytes(int B, int Hq, int Hkv, int Qmax, int D,
+                                         int max_seq_len, int partition_tokens, int num_sms) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Qmax < 1 || Qmax > kMaxQmax || max_seq_len < 1)
+    return VAE4_ERR_SHAPE;
+  if (D != 64 && D != 128 && D != 256) return VAE4_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return VAE4_ERR_GQA;
+  const int64_t rows_pad = align_up((int64_t)Qmax * (Hq / Hkv), 16);
+  if (rows_pad > kMaxRowsPad) return VAE4_ERR_UNSUPPORTED;
+  int sms = num_sms;
+  if (sms < 0) return VAE4_ERR_SHAPE;
+  if (sms == 0) {
+    const int rc = device_sms(&sms);
+    if (rc) return rc;
+  }
+  int T = 0, P = 0;
+  const int rc = do_plan(B, Hkv, max_seq_len, partition_tokens, sms, &T, &P);
+  if (rc) return rc;
+  return ws_layout(B, Hkv, P, (int)rows_pad, D).total;
+}
+
+int verify_attn_e4m3_abi_version(void) { return VAE4_ABI_VERSION; }
+
+const char *verify_attn_e4m3_strerror(int code) {
+  switch (code) {
+    case VAE4_OK: return "ok";
+    case VAE4_ERR_NULL: return "a required pointer is NULL";
+    case VAE4_ERR_DTYPE: return "wrong dtype";
+    case VAE4_ERR_SHAPE: return "inconsistent or out-of-range shape";
+    case VAE4_ERR_STRIDE: return "unsupported strides";
+    case VAE4_ERR_MISALIGNED: return "base address or row not 16-byte aligned";
+    case VAE4_ERR_UNSUPPORTED: return "head dim, page size or row count not supported";
+    case VAE4_ERR_GQA: return "q heads not a multiple of KV heads";
+    case VAE4_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case VAE4_ERR_CUDA: return "CUDA runtime error";
+    case VAE4_ERR_PARTITION: return "partition_tokens must be a positive multiple of 16 giving at most 8192 partitions";
+    case VAE4_ERR_OPTIONS: return "invalid options";
+    default: return "unknown error";
+  }
+}
+
+int verify_attn_e4m3_read_status(const vae4_tensor *workspace, int32_t *host_status,
+                                 vae4_stream stream) {
+  if (!workspace || !workspace->data || !host_status) return VAE4_ERR_NULL;
+  if (workspace->dtype != VAE4_U8) return VAE4_ERR_DTYPE;
+  if (workspace->ndim != 1 || workspace->shape[0] < kStatusBytes) return VAE4_ERR_WORKSPACE;
+  if (cudaMemcpyAsync(host_status, workspace->data, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+int verify_attn_e4m3_clear_status(const vae4_tensor *workspace, vae4_stream stream) {
+  if (!workspace || !workspace->data) return VAE4_ERR_NULL;
+  if (workspace->dtype != VAE4_U8) return VAE4_ERR_DTYPE;
+  if (workspace->ndim != 1 || workspace->shape[0] < kStatusBytes) return VAE4_ERR_WORKSPACE;
+  if (cudaMemsetAsync(workspace->data, 0, sizeof(int32_t),
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2, vae4_stream stream) {
+  if (!dev_out || !scale_log2) return VAE4_ERR_NULL;
+  if (!al16(dev_out)) return VAE4_ERR_MISALIGNED;
+  *scale_log2 = -8;
+  if (vae4::launch_decode_table(static_cast<uint16_t *>(dev_out),
+                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,175 @@
+// Combine kernel: merges the FP32 partition states of each output row in
+// ascending partition order and writes the FP16 output.
+//
+// For row r of (sequence b, KV head h), over the live partitions p (those
+// with p*T < L and a nonzero running sum):
+//     M   = max_p m_p                  (m_p in log2 units of the score)
+//     w_p = 2^(m_p - M)
+//     out = (sum_p w_p O_p) / (sum_p w_p l_p) * s_V * 2^8
+// all in FP32, rounded once to FP16 (round to nearest even), with a fixed
+// summation order.  This is the
+// single "final combine" of the FP32 max/sum/unnormalised-PV state (PR #524
+// "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32 partials",
+// final status; "FP32 scalar partial storage/reduction", PR #560, Purpose).
+// Padding query slots, dead sequences (L == 0) and sequences whose lengths
+// or pages were invalid get zeros.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace vae4 {
+
+namespace {
+
+constexpr int kCombineThreads = 256;
+
+// One CTA per output row (r, h, b).  Partition weights are computed once into
+// shared memory; the P.V partials are then summed by kCombineThreads/(D/4)
+// groups of threads, group k taking partitions k, k+ngrp, ... in ascending
+// order, and the group sums are added in group order: a fixed summation order
+// that does not depend on scheduling, so repeated runs agree bit for bit.
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+  extern __shared__ __align__(16) float csm[];
+  constexpr int LANES = D / 4;                      // float4 lanes per row
+  constexpr int NGRP = kCombineThreads / LANES;     // partition groups
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float4 accs[NGRP][LANES];
+
+  // wait until the split kernel's partials are complete and visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+  const int r = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = r / p.G, g = r - i * p.G;
+  __half *out = static_cast<__half *>(p.out) + (int64_t)b * p.o_sb + (int64_t)i * p.o_si +
+                (int64_t)(h * p.G + g) * p.o_sh;
+
+  const int L = p.seq[(int64_t)b * p.seq_sb];
+  const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
+  const bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql;
+  const int nP = dead ? 0 : (L + p.T - 1) / p.T;
+
+  float *wm = csm;       // m_p, then the weight w_p
+  float *wl = csm + p.P; // l_p
+  const int64_t pstride = (int64_t)p.rows_pad;
+  const float *ml = p.ws_ml + (int64_t)(b * p.Hkv + h) * p.P * pstride * 2 + r * 2;
+  const float kNegInf = -__int_as_float(0x7f800000);
+
+  // ---- pass 1: load (m_p, l_p), maximum over partitions with l_p > 0
+  float mx = kNegInf;
+  bool bad = false;
+  for (int q = tid; q < nP; q += kCombineThreads) {
+    const float2 v = *reinterpret_cast<const float2 *>(ml + q * pstride * 2);
+    wm[q] = v.x;
+    wl[q] = v.y;
+    if (v.y < 0.f) bad = true;  // a partition met an invalid page
+    if (v.y > 0.f) mx = fmaxf(mx, v.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  const bool any_bad = __syncthreads_or(bad);
+  float M = red[0];
+#pragma unroll
+  for (int k = 1; k < kCombineThreads / 32; ++k) M = fmaxf(M, red[k]);
+  __syncthreads();
+
+  // ---- pass 2: weights w_p = 2^(m_p - M) and the total sum (fixed tree)
+  float lam = 0.f;
+  for (int q = tid; q < nP; q += kCombineThreads) {
+    const float l = wl[q];
+    const float w = l > 0.f ? (wm[q] == M ? 1.f : exp2f(wm[q] - M)) : 0.f;
+    wm[q] = w;
+    lam += w * l;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, o);
+  if (lane == 0) red[warp] = lam;
+  __syncthreads();
+  float Lam = 0.f;
+#pragma unroll
+  for (int k = 0; k < kCombineThreads / 32; ++k) Lam += red[k];
+
+  // ---- pass 3: sum of w_p * O_p per group, then over groups
+  const int l4 = tid % LANES, grp = tid / LANES;
+  const float *o = p.ws_o + (int64_t)(b * p.Hkv + h) * p.P * pstride * D + (int64_t)r * D + 4 * l4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int q = grp; q < nP; q += NGRP) {
+    const float w = wm[q];
+    const float4 v = *reinterpret_cast<const float4 *>(o + q * pstride * D);
+    acc.x += w * v.x;
+    acc.y += w * v.y;
+    acc.z += w * v.z;
+    acc.w += w * v.w;
+  }
+  accs[grp][l4] = acc;
+  __syncthreads();
+  if (grp != 0) return;
+  float4 s = accs[0][l4];
+#pragma unroll
+  for (int k = 1; k < NGRP; ++k) {
+    const float4 v = accs[k][l4];
+    s.x += v.x;
+    s.y += v.y;
+    s.z += v.z;
+    s.w += v.w;
+  }
+  uint2 res = make_uint2(0u, 0u);
+  if (!dead && !any_bad && Lam > 0.f) {
+    const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // V holds dec*2^-8
+    const __half2 lo = __floats2half2_rn(__fdiv_rn(s.x, Lam) * beta, __fdiv_rn(s.y, Lam) * beta);
+    const __half2 hi = __floats2half2_rn(__fdiv_rn(s.z, Lam) * beta, __fdiv_rn(s.w, Lam) * beta);
+    res.x = *reinterpret_cast<const uint32_t *>(&lo);
+    res.y = *reinterpret_cast<const uint32_t *>(&hi);
+  }
+  *reinterpret_cast<uint2 *>(out + 4 * l4) = res;
+}
+
+__global__ void decode_table_kernel(uint16_t *out) {
+  const int t = threadIdx.x;  // 64 threads x 4 codes
+  const uint32_t w = (uint32_t)(4 * t) | (uint32_t)(4 * t + 1) << 8 | (uint32_t)(4 * t + 2) << 16 |
+                     (uint32_t)(4 * t + 3) << 24;
+  uint32_t lo, hi;
+  e4m3x4_to_f16x4(w, lo, hi);
+  out[4 * t + 0] = (uint16_t)(lo & 0xFFFFu);
+  out[4 * t + 1] = (uint16_t)(lo >> 16);
+  out[4 * t + 2] = (uint16_t)(hi & 0xFFFFu);
+  out[4 * t + 3] = (uint16_t)(hi >> 16);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.Qmax * p.G, p.Hkv, p.B);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int smem = (int)cfg.dynamicSmemBytes;
+  switch (p.D) {
+    case 64:
+      cudaFuncSetAttribute(combine_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      return cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
+    case 128:
+      cudaFuncSetAttribute(combine_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      return cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
+    case 256:
+      cudaFuncSetAttribute(combine_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      return cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_table(uint16_t *out, cudaStream_t stream) {
+  decode_table_kernel<<<1, 64, 0, stream>>>(out);
+  return cudaGetLastError();
+}
+
+}  // namespace vae4

@@ -1,0 +1,48 @@
+// Launch parameters shared by the host entry points and the kernels.
+#pragma once
+
+#include <stdint.h>
+
+namespace vae4 {
+
+// Everything a split (partition) kernel needs.  Strides are in elements.
+struct SplitParams {
+  const void *q;        // fp16 [B][Qmax][Hq][D]
+  int64_t q_sb, q_si, q_sh;
+  const uint8_t *kv;    // u8 [n_pages][2][Hkv][page][D]
+  int64_t n_pages;
+  const int32_t *bt;    // i32 [B][max_pages]
+  int64_t bt_sb;
+  int32_t max_pages;
+  const int32_t *seq;   // i32 [B] or [B][2]
+  int32_t seq_sb;       // stride of dim 0
+  int32_t seq_has_qlen; // 1 if [B][2]
+  const float *scales;  // f32 [Hkv][2], row stride scale_sh
+  int32_t scale_sh;
+  float *ws_ml;         // f32 [B][Hkv][P][rows_pad][2]
+  float *ws_o;          // f32 [B][Hkv][P][rows_pad][D]
+  uint32_t *status;     // sticky status word
+  int32_t B, Qmax, Hq, Hkv, G, D, page;
+  int32_t rows;         // Qmax * G
+  int32_t rows_pad;     // rows rounded up to 16
+  int32_t T;            // partition tokens
+  int32_t P;            // partitions per (b, h)
+  int32_t capacity;     // launch capacity (tokens)
+  float sm_scale;       // softmax scale
+};
+
+// The combine kernel's parameters.
+struct CombineParams {
+  const float *ws_ml;
+  const float *ws_o;
+  void *out;            // fp16 [B][Qmax][Hq][D]
+  int64_t o_sb, o_si, o_sh;
+  const int32_t *seq;
+  int32_t seq_sb, seq_has_qlen;
+  const float *scales;
+  int32_t scale_sh;
+  int32_t B, Qmax, Hq, Hkv, G, D;
+  int32_t rows_pad, T, P, capacity;
+};
+
+}  // namespace vae4

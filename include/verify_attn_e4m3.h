@@ -1,0 +1,238 @@
+/*
+ * verify_attn_e4m3.h -- C ABI of the GB300 (sm_103a) paged grouped-query
+ * verify attention over an FP8 E4M3 KV cache with FP32 split-K state.
+ *
+ * The operation (sources: the 1Cat-vLLM pull-request pages
+ *   PR #560 "[Bugfix] Use FP32 state and E4M3 defaults for DFlash2",
+ *   PR #566 "[Kernel] Finalize the audited TP2 DFlash2 31/29 ms endpoint",
+ *   PR #524 "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32
+ *            partials"):
+ *
+ *   For sequence b with L = seq_len[b] cached tokens whose last q = q_len[b]
+ *   positions are the draft tokens being verified, query i (0 <= i < q) of q
+ *   head hq attends causally to keys 0 .. L-q+i of KV head h = hq / (Hq/Hkv)
+ *   (dense q2-8 "GQA6/D256" with "per-query device lengths", PR #524, Scope
+ *   and non-duplication; q1 and q16 per PR #560, Purpose and Test Plan):
+ *
+ *     z_j  = softmax_scale * sum_d Q[b,i,hq,d] * dec(K_j[d]) * s_K[h]
+ *     out  = sum_j exp(z_j - max z) * dec(V_j[d]) * s_V[h] / sum_j exp(z_j - max z)
+ *
+ *   dec() is the exact E4M3 (OCP E4M3FN) decode ("exact E4M3 decoder", PR
+ *   #566, Final audit); s_K, s_V are per-KV-head FP32 scales ("KV scaling",
+ *   PR #560, Test Plan and Results).  The KV storage stays FP8 and the tensor
+ *   core operands FP16 (PR #560, Purpose).  The context is split into
+ *   partitions whose state -- running max, running sum and unnormalised P.V
+ *   -- stays FP32 until one final FP32 combine in ascending partition order
+ *   (PR #524, final status: "FP32 max/sum and unnormalized PV until the
+ *   final combine"; PR #560, Purpose: "FP32 ... partial storage/reduction").
+ *
+ * Conventions of every entry point:
+ *   - All tensor data pointers are DEVICE pointers unless stated otherwise.
+ *     Strides are in elements.  The library never allocates or frees device
+ *     memory: the caller owns every buffer, including the workspace.
+ *   - Calls are asynchronous on `stream` and never synchronise the host, so
+ *     they can be captured in a CUDA graph.  Lengths, block table and scales
+ *     are read on the device, so they may change between graph replays.
+ *   - A workspace serves one call in flight at a time: use one workspace per
+ *     concurrently executing stream ("dtype-separated workspaces", PR #560,
+ *     Test Plan and Results).
+ *   - Argument errors are returned as negative codes before anything is
+ *     launched.  Data errors only visible on the device (block id out of
+ *     range, a length beyond capacity, q_len > L, a bounded wait that ran
+ *     out) set bits in a sticky status word inside the workspace and zero
+ *     the affected sequence's output; nothing traps or aborts.
+ */
+#ifndef VERIFY_ATTN_E4M3_H_
+#define VERIFY_ATTN_E4M3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI revision.  A wrapper refuses a library whose revision differs from the
+ * one it was written for ("stale libraries fail closed", PR #524, Scope and
+ * non-duplication; "Precision revision 4 ... Older binaries cannot silently
+ * fall back", PR #560, Purpose). */
+#define VAE4_ABI_VERSION 1
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *vae4_stream;
+
+enum vae4_dtype {
+  VAE4_U8 = 1,  /* E4M3 bytes */
+  VAE4_I32 = 2,
+  VAE4_F16 = 3,
+  VAE4_F32 = 4
+};
+
+/* A strided view.  `data` is a device pointer unless an entry point says
+ * otherwise; shape/stride entries beyond ndim are ignored. */
+typedef struct {
+  void *data;
+  int32_t dtype; /* enum vae4_dtype */
+  int32_t ndim;
+  int64_t shape[5];
+  int64_t stride[5]; /* elements */
+} vae4_tensor;
+
+/* Optional parameters of verify_attn_e4m3_ex (zero-initialise for defaults). */
+typedef struct {
+  float softmax_scale;      /* 0 -> 1/sqrt(D) */
+  int32_t partition_tokens; /* split-K partition length T (multiple of 16);
+                               0 -> automatic plan from the capacity */
+  int32_t max_seq_len;      /* launch capacity in tokens; 0 ->
+                               block_table columns * page size */
+  int32_t num_sms;          /* SMs the plan targets; 0 -> current device */
+  int32_t flags;            /* reserved, must be 0 */
+} vae4_options;
+
+/* Return codes. */
+enum vae4_error {
+  VAE4_OK = 0,
+  VAE4_ERR_NULL = -1,        /* a required pointer is NULL */
+  VAE4_ERR_DTYPE = -2,       /* a tensor has the wrong dtype */
+  VAE4_ERR_SHAPE = -3,       /* inconsistent or out-of-range shapes */
+  VAE4_ERR_STRIDE = -4,      /* unsupported strides (see each argument) */
+  VAE4_ERR_MISALIGNED = -5,  /* a base address or row is not 16-byte aligned */
+  VAE4_ERR_UNSUPPORTED = -6, /* D, page size or rows outside the kernels' set */
+  VAE4_ERR_GQA = -7,         /* Hq is not a multiple of Hkv */
+  VAE4_ERR_WORKSPACE = -8,   /* workspace too small or misaligned */
+  VAE4_ERR_CUDA = -9,        /* a CUDA runtime call failed */
+  VAE4_ERR_PARTITION = -10,  /* partition_tokens not a positive multiple of 16,
+                                or more than 8192 partitions per sequence */
+  VAE4_ERR_OPTIONS = -11     /* nonzero reserved option flags */
+};
+
+/* Bits of the device status word (sticky until verify_attn_e4m3_clear_status). */
+#define VAE4_STATUS_BAD_BLOCK 0x1u  /* block id < 0 or >= number of pages */
+#define VAE4_STATUS_BAD_LENGTH 0x2u /* L < 0 or L > launch capacity */
+#define VAE4_STATUS_BAD_QLEN 0x4u   /* q_len < 0, q_len > Qmax, or q_len > L > 0 */
+#define VAE4_STATUS_TIMEOUT 0x8u    /* a bounded pipeline wait ran out */
+
+/*
+ * verify_attn_e4m3 -- the verify step (split kernel + combine kernel).
+ *
+ *  q           F16 [B][Qmax][Hq][D]; D in {64, 128, 256}; Qmax <= 16;
+ *              stride[3] == 1, other strides multiples of 8 elements, base
+ *              16-byte aligned (a misaligned view is rejected, never copied;
+ *              cf. the Q-base safety repair of PR #524, final status).  Slot
+ *              i of sequence b is a query only if i < q_len[b]; the other
+ *              slots are padding and are never read.
+ *  kv_pages    U8 [n_pages][2][Hkv][page][D], contiguous; index 0 of dim 1
+ *              is K, 1 is V; page in {16, 32, 64, 128} tokens; base 16-byte
+ *              aligned.  Each (page, K|V, head) slice of page*D bytes is one
+ *              contiguous 16-byte-aligned block.
+ *  block_table I32 [B][max_pages], stride[1] == 1: logical page j of
+ *              sequence b lives in physical page block_table[b][j].  Only
+ *              the first ceil(L/page) entries of a row are read.
+ *  seq_lens    I32 [B] (L; q_len = Qmax for every sequence) or I32 [B][2]
+ *              with stride[1] == 1 holding (L, q_len).  L counts the q tail.
+ *              L == 0 marks a dead sequence (all-zero output, no status bit).
+ *  kv_scales   F32 [Hkv][2] = (s_K, s_V), stride[1] == 1.
+ *  out         F16, same shape as q, same stride rules; written in full
+ *              (padding slots and dead sequences get zeros).  Must not
+ *              overlap any input.
+ *  workspace   U8 [bytes], bytes >= verify_attn_e4m3_workspace_bytes(...),
+ *              base 256-byte aligned.  Holds the FP32 partials and the
+ *              status word.  Zero-fill it (or call
+ *              verify_attn_e4m3_clear_status) once before first use.
+ *  stream      CUDA stream of the current device.
+ *
+ * Returns VAE4_OK or a negative vae4_error; on error nothing is launched.
+ */
+int verify_attn_e4m3(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                     const vae4_tensor *block_table, const vae4_tensor *seq_lens,
+                     const vae4_tensor *kv_scales, const vae4_tensor *out,
+                     const vae4_tensor *workspace, vae4_stream stream);
+
+/* As verify_attn_e4m3, with options (NULL = defaults). */
+int verify_attn_e4m3_ex(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                        const vae4_tensor *block_table, const vae4_tensor *seq_lens,
+                        const vae4_tensor *kv_scales, const vae4_tensor *out,
+                        const vae4_tensor *workspace, vae4_stream stream,
+                        const vae4_options *opt);
+
+/*
+ * The two stages of verify_attn_e4m3, for callers that schedule them apart
+ * (e.g. to time or overlap them).  Same arguments and contract.
+ *   verify_attn_e4m3_partials: the split kernel only -- writes each live
+ *     partition's FP32 (max, sum, unnormalised P.V) into the workspace.
+ *   verify_attn_e4m3_combine: the combine kernel only -- reads the partials
+ *     of the same arguments from the workspace and writes `out`.  It must
+ *     follow a verify_attn_e4m3_partials call with identical arguments on
+ *     the same stream; q and kv_pages are not read.
+ */
+int verify_attn_e4m3_partials(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                              const vae4_tensor *block_table,
+                              const vae4_tensor *seq_lens,
+                              const vae4_tensor *kv_scales, const vae4_tensor *out,
+                              const vae4_tensor *workspace, vae4_stream stream,
+                              const vae4_options *opt);
+int verify_attn_e4m3_combine(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                             const vae4_tensor *block_table,
+                             const vae4_tensor *seq_lens,
+                             const vae4_tensor *kv_scales, const vae4_tensor *out,
+                             const vae4_tensor *workspace, vae4_stream stream,
+                             const vae4_options *opt);
+
+/*
+ * verify_attn_e4m3_plan -- the split-K partition plan (host only, no CUDA).
+ * Partition p of every sequence covers tokens [p*T, min((p+1)*T, L)); the
+ * launch has P = ceil(max_seq_len / T) partitions per (sequence, KV head).
+ * With partition_tokens == 0, T is the smallest multiple of 16 for which
+ * B*Hkv*P does not exceed max(num_sms, B*Hkv) (one wave on the SMs; the
+ * pages' split used one partition per V100 SM: the 80 of the [80,8,6,2]
+ * workspace, PR #524, final status).  num_sms must be > 0.
+ * Returns VAE4_OK, VAE4_ERR_SHAPE or VAE4_ERR_PARTITION.
+ */
+int verify_attn_e4m3_plan(int B, int Hkv, int max_seq_len, int partition_tokens,
+                          int num_sms, int32_t *partition_tokens_out,
+                          int32_t *partitions_out);
+
+/*
+ * verify_attn_e4m3_workspace_bytes -- bytes of workspace a call with these
+ * sizes needs: the status word, FP32 (max, sum) per partition and row
+ * ([B][Hkv][P][rows][2], the pages' [80,8,6,2] "max/sum" layout, PR #524,
+ * final status) and the FP32 unnormalised P.V per partition and row
+ * ([B][Hkv][P][rows][D]); rows = Qmax * Hq/Hkv rounded up to 16.
+ * num_sms == 0 queries the current device (a CUDA call); any other value
+ * makes this a pure host computation.  Returns the size, or a negative
+ * vae4_error.
+ */
+int64_t verify_attn_e4m3_workspace_bytes(int B, int Hq, int Hkv, int Qmax, int D,
+                                         int max_seq_len, int partition_tokens,
+                                         int num_sms);
+
+/* VAE4_ABI_VERSION of the built library. */
+int verify_attn_e4m3_abi_version(void);
+
+/* Static string for a vae4_error code. */
+const char *verify_attn_e4m3_strerror(int code);
+
+/* Copy the status word of `workspace` into *host_status (host pointer) with
+ * an asynchronous copy on `stream`; read it after synchronising the stream. */
+int verify_attn_e4m3_read_status(const vae4_tensor *workspace,
+                                 int32_t *host_status, vae4_stream stream);
+
+/* Zero the status word of `workspace` on `stream`. */
+int verify_attn_e4m3_clear_status(const vae4_tensor *workspace, vae4_stream stream);
+
+/*
+ * verify_attn_e4m3_decode_table -- test hook for the exact decoder: runs the
+ * kernels' E4M3 -> FP16 decode routine on all 256 byte codes and writes the
+ * raw FP16 bit patterns to dev_out (device, 256 x uint16).  The decoder maps
+ * byte b to dec(b) * 2^scale_log2 exactly; *scale_log2 (host pointer)
+ * receives that exponent (the kernels fold 2^-scale_log2 into their FP32
+ * scales).  NaN codes 0x7F / 0xFF decode to a finite pattern and are outside
+ * the contract.  ("exhaustive E4M3 bytes", PR #566, Test Result.)
+ */
+int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2,
+                                  vae4_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VERIFY_ATTN_E4M3_H_ */

@@ -1,0 +1,174 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol,
+reports its ABI revision, plans partitions, sizes workspaces and rejects bad
+arguments before touching CUDA.  No compute call is made here."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import fp8_paged_attention_e4m3_gb300 as vae4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "verify_attn_e4m3.h")
+GOLD = json.load(open(os.path.join(ROOT, "tests", "golden", "page_sizes.json")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return vae4.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(verify_attn_e4m3\w*)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert declared and set(declared) == set(vae4.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_strerror(lib):
+    assert lib.verify_attn_e4m3_abi_version() == vae4.ABI_VERSION
+    for code, name in vae4.ERRORS.items():
+        assert vae4.strerror(code) and vae4.strerror(code) != "unknown error", name
+    assert vae4.strerror(-999) == "unknown error"
+
+
+@pytest.mark.parametrize("B,Hkv,cap,sms,T,P", [
+    (1, 1, 262144, 152, 1728, 152),   # long context: one partition per SM
+    (1, 1, 131072, 152, 864, 152),    # TP4 shard
+    (4, 2, 262144, 152, 13808, 19),   # TP2 shard: 8 units x 19 partitions
+    (1, 1, 1024, 152, 64, 16),        # never below 64 tokens
+    (200, 1, 5000, 152, 5008, 1),     # more units than SMs: one partition each
+])
+def test_auto_plan(B, Hkv, cap, sms, T, P):
+    assert vae4.plan(B, Hkv, cap, 0, sms) == (T, P)
+    assert B * Hkv * P <= max(sms, B * Hkv)
+
+
+def test_explicit_plan_and_errors():
+    assert vae4.plan(1, 1, 1024, 256, 152) == (256, 4)   # tiny: 4 partitions
+    assert vae4.plan(1, 1, 1025, 256, 152) == (256, 5)
+    for bad in (-16, 8, 100):
+        with pytest.raises(vae4.Vae4Error):
+            vae4.plan(1, 1, 1024, bad, 152)
+    assert vae4.plan(1, 1, 131072, 16, 152) == (16, 8192)
+    with pytest.raises(vae4.Vae4Error):             # more than 8192 partitions
+        vae4.plan(1, 1, 262144, 16, 152)
+
+
+def test_workspace_matches_the_pages_max_sum_layout():
+    g = GOLD["max_sum_workspace"]
+    P, q, G, D = g["partitions"], g["queries"], g["group_heads"], g["head_dim"]
+    T = 3296  # 80 partitions of 3296 tokens cover 262144 (the pages' page3296)
+    assert vae4.plan(1, 1, 262144, T, 80) == (T, P)
+    n = vae4.workspace_bytes(1, G, 1, q, D, 262144, T, 80)
+    ml = 1
+    for s in g["new_shape"]:
+        ml *= s
+    ml *= g["element_bytes"]
+    assert ml - g["delta_bytes"] == 80 * 8 * 6 * 4            # the old [80,8,6]
+    o = P * q * G * D * 4                                     # FP32 unnormalised PV
+    assert n == 256 + ml + o                                  # status + (max,sum) + PV
+    qc = GOLD["q_copy"]
+    assert qc["shape"][0] * qc["shape"][1] * qc["shape"][2] * qc["element_bytes"] == qc["max_bytes"]
+
+
+def test_workspace_errors():
+    with pytest.raises(vae4.Vae4Error):
+        vae4.workspace_bytes(1, 6, 4, 8, 256, 1000, 0, 152)   # GQA mismatch
+    with pytest.raises(vae4.Vae4Error):
+        vae4.workspace_bytes(1, 6, 1, 8, 96, 1000, 0, 152)    # unsupported D
+    with pytest.raises(vae4.Vae4Error):
+        vae4.workspace_bytes(1, 12, 1, 16, 256, 1000, 0, 152)  # 192 rows > 96
+    assert vae4.workspace_bytes(1, 6, 1, 16, 256, 1000, 0, 152) > 0  # q16 x G6 = 96
+
+
+# -------------------------------------------------- argument validation
+FAKE = 0x100000  # never dereferenced: every case below fails validation
+
+
+def _t(dtype, shape, strides=None, data=FAKE):
+    d = vae4.Tensor()
+    d.data = data
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    for k, (s, st) in enumerate(zip(shape, strides)):
+        d.shape[k] = s
+        d.stride[k] = st
+    return d
+
+
+def _args(**over):
+    B, Q, Hq, Hkv, D, page, npg, mp = 1, 8, 6, 1, 256, 16, 80, 64
+    a = dict(
+        q=_t(vae4.VAE4_F16, [B, Q, Hq, D]),
+        kv=_t(vae4.VAE4_U8, [npg, 2, Hkv, page, D]),
+        bt=_t(vae4.VAE4_I32, [B, mp]),
+        seq=_t(vae4.VAE4_I32, [B, 2]),
+        sc=_t(vae4.VAE4_F32, [Hkv, 2]),
+        out=_t(vae4.VAE4_F16, [B, Q, Hq, D], data=FAKE * 2),
+        ws=_t(vae4.VAE4_U8, [1 << 24], data=FAKE * 4),
+    )
+    a.update(over)
+    return a
+
+
+def _call(lib, a, opt=None):
+    o = opt or vae4.Options(0.0, 0, 0, 152, 0)
+    return lib.verify_attn_e4m3_ex(*[ctypes.byref(a[k]) for k in
+                                     ("q", "kv", "bt", "seq", "sc", "out", "ws")],
+                                   None, ctypes.byref(o))
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=_t(vae4.VAE4_F32, [1, 8, 6, 256])), -2),
+    (dict(q=_t(vae4.VAE4_F16, [1, 8, 6, 96])), -3),                 # out shape differs
+    (dict(q=_t(vae4.VAE4_F16, [1, 8, 6, 256], data=FAKE + 2)), -5), # half-offset view
+    (dict(q=_t(vae4.VAE4_F16, [1, 8, 6, 256], [12288, 1536, 256, 2])), -4),
+    (dict(q=_t(vae4.VAE4_F16, [1, 8, 6, 256], [12290, 1536, 256, 1])), -4),
+    (dict(kv=_t(vae4.VAE4_U8, [80, 2, 1, 24, 256])), -6),           # page 24
+    (dict(kv=_t(vae4.VAE4_U8, [80, 2, 4, 16, 256])), -7),           # 6 % 4
+    (dict(kv=_t(vae4.VAE4_U8, [80, 2, 1, 16, 256], data=FAKE + 8)), -5),
+    (dict(kv=_t(vae4.VAE4_U8, [80, 2, 1, 16, 256], [8448, 4224, 4224, 264, 1])), -4),
+    (dict(bt=_t(vae4.VAE4_F32, [1, 64])), -2),
+    (dict(bt=_t(vae4.VAE4_I32, [2, 64])), -3),
+    (dict(seq=_t(vae4.VAE4_I32, [1, 3])), -3),
+    (dict(sc=_t(vae4.VAE4_F32, [2, 2])), -3),
+    (dict(ws=_t(vae4.VAE4_U8, [1 << 24], data=FAKE + 16)), -8),
+    (dict(ws=_t(vae4.VAE4_U8, [1000], data=FAKE * 4)), -8),
+])
+def test_validation_rejects(lib, over, code):
+    assert _call(lib, _args(**over)) == code
+
+
+def test_validation_options(lib):
+    assert _call(lib, _args(), vae4.Options(0.0, 24, 0, 152, 0)) == -10
+    assert _call(lib, _args(), vae4.Options(0.0, 0, 0, 152, 1)) == -11
+    assert _call(lib, _args(), vae4.Options(-1.0, 0, 0, 152, 0)) == -11
+    # capacity beyond what the block table can address
+    assert _call(lib, _args(), vae4.Options(0.0, 0, 64 * 16 + 1, 152, 0)) == -3
+    a = _args()
+    a["q"].data = None
+    assert _call(lib, a) == -1
+
+
+def test_stride_counterexample_is_rejected(lib):
+    """The pages' 8-but-not-16-byte token stride (264 B) cannot be expressed:
+    the pool must be contiguous, so each (page, K|V, head) slice starts on a
+    16-byte boundary; a 264-byte token stride is a stride error."""
+    g = GOLD["stride_counterexample"]
+    assert g["strides"][1] == g["second_token_byte"] and g["second_token_byte"] % 16 == 8
+    kv = _t(vae4.VAE4_U8, [80, 2, 1, 16, 256], [2 * 16 * 264, 16 * 264, 16 * 264, 264, 1])
+    assert _call(lib, _args(kv=kv)) == -4

@@ -278,18 +278,18 @@ def sample_rows(w: Workload, n: int, seed: int = 0, seq_len=None, q_len=None):
     return np.asarray(rows, dtype=np.int32)
 
 
-# Exact outputs of midpoint_case(): 0.25 + 2^-13 (d < 8) and 0.25 + 3*2^-13
-# (d >= 8), each the midpoint of two adjacent fp16 values.
+# Exact outputs of midpoint_case(): 0.25 + 2^-13 (d < D/2) and 0.25 + 3*2^-13
+# (d >= D/2), each the midpoint of two adjacent fp16 values.
 MIDPOINT_VALUES = (0.25 + 2.0 ** -13, 0.25 + 3 * 2.0 ** -13)
 
 
-def midpoint_case(n: int = 1024) -> Workload:
+def midpoint_case(n: int = 1024, D: int = 64) -> Workload:
     """One query, zero Q (every score equal), n keys.  Even keys hold V bytes
-    0x78 (256), odd keys 0x20 (0.125) in columns 0..7 and 0x2C (0.375) in
-    columns 8..15; s_V = 2^-9.  The mean over all n keys is then
+    0x78 (256), odd keys 0x20 (0.125) in columns 0..D/2-1 and 0x2C (0.375) in
+    columns D/2..D-1; s_V = 2^-9.  The mean over all n keys is then
     (256 + 0.125) / 2 * 2^-9 and (256 + 0.375) / 2 * 2^-9: exact fp16
     midpoints (the first rounds down to even, the second up)."""
-    w = custom("midpoint", B=1, Qmax=1, Hq=1, Hkv=1, D=16, seq_lens=[n],
+    w = custom("midpoint", B=1, Qmax=1, Hq=1, Hkv=1, D=D, seq_lens=[n],
                q_lens=[1], seed=9)
     w.q[:] = 0
     w.kv_scales[:, 1] = np.float32(2.0 ** -9)
@@ -299,6 +299,20 @@ def midpoint_case(n: int = 1024) -> Workload:
         if j % 2 == 0:
             w.kv_pages[p, 1, 0, s, :] = 0x78
         else:
-            w.kv_pages[p, 1, 0, s, :8] = 0x20
-            w.kv_pages[p, 1, 0, s, 8:] = 0x2C
+            w.kv_pages[p, 1, 0, s, :D // 2] = 0x20
+            w.kv_pages[p, 1, 0, s, D // 2:] = 0x2C
     return w
+
+
+def to_device(w: Workload, device="cuda", seq_len=None, q_len=None):
+    """The workload's inputs as device tensors for the library:
+    (q, kv_pages, block_table, seq_lens [B][2] = (L, q_len), kv_scales)."""
+    import torch
+    sl = w.seq_len if seq_len is None else seq_len
+    ql = w.q_len if q_len is None else q_len
+    seq = np.stack([np.asarray(sl, np.int32), np.asarray(ql, np.int32)], axis=1)
+    return (torch.from_numpy(w.q).to(device),
+            torch.from_numpy(w.kv_pages).to(device),
+            torch.from_numpy(w.block_table).to(device),
+            torch.from_numpy(np.ascontiguousarray(seq)).to(device),
+            torch.from_numpy(w.kv_scales).to(device))
