@@ -35,7 +35,10 @@ EXPORTS = (
     "verify_attn_e4m3_workspace_bytes", "verify_attn_e4m3_abi_version",
     "verify_attn_e4m3_strerror", "verify_attn_e4m3_read_status",
     "verify_attn_e4m3_clear_status", "verify_attn_e4m3_decode_table",
+    "verify_attn_e4m3_noalloc",
 )
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class Tensor(ctypes.Structure):
@@ -107,6 +110,9 @@ def load(build_if_stale: bool = True):
                                                       ctypes.POINTER(ctypes.c_int32),
                                                       ctypes.c_void_p]
         lib.verify_attn_e4m3_decode_table.restype = ctypes.c_int
+        lib.verify_attn_e4m3_noalloc.argtypes = [P] * 6 + [ctypes.c_void_p,
+                                                           ctypes.POINTER(Options)]
+        lib.verify_attn_e4m3_noalloc.restype = ctypes.c_int
         v = lib.verify_attn_e4m3_abi_version()
         if v != ABI_VERSION:
             raise RuntimeError(f"stale library: ABI revision {v}, binding expects "
@@ -206,6 +212,24 @@ def verify_attn_e4m3_partials(*args, **kw):
 def verify_attn_e4m3_combine(*args, **kw):
     """Combine stage only (see the header)."""
     return _stage("verify_attn_e4m3_combine", *args, **kw)
+
+
+def verify_attn_e4m3_noalloc(q, kv_pages, block_table, seq_lens, kv_scales, out, *,
+                             softmax_scale: float = 0.0, partition_tokens: int = 0,
+                             max_seq_len: int = 0, num_sms: int = 0, stream=None):
+    """The verify step without a workspace, for callers that cannot allocate
+    device memory: the library's own fixed 8 MiB scratch holds the partials.
+    Calls on one device share that scratch, so they must not overlap on the
+    GPU; the first call on a device must precede any stream capture."""
+    lib = load()
+    opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
+                  int(num_sms), 0)
+    descs = [describe(t) for t in (q, kv_pages, block_table, seq_lens, kv_scales, out)]
+    rc = lib.verify_attn_e4m3_noalloc(*[ctypes.byref(x) for x in descs],
+                                      ctypes.c_void_p(_stream_handle(stream)),
+                                      ctypes.byref(opt))
+    _check(rc, "verify_attn_e4m3_noalloc")
+    return out
 
 
 def verify_attn_e4m3_plan(B: int, Hkv: int, max_seq_len: int, partition_tokens: int = 0,

@@ -232,6 +232,49 @@ int verify_attn_e4m3_clear_status(const vae4_tensor *workspace, vae4_stream stre
 int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2,
                                   vae4_stream stream);
 
+/* Bytes of the library-owned scratch that verify_attn_e4m3_noalloc uses. */
+#define VAE4_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * verify_attn_e4m3_noalloc -- the verify step for callers that cannot
+ * allocate device memory.  (No counterpart on the pages: this is an
+ * addition of this library.)
+ *
+ * Some callers have no way to hand over a workspace: code that runs where a
+ * device allocation is forbidden or unsafe -- inside a region being
+ * captured into a CUDA graph, inside a plugin or custom-op callback whose
+ * host framework owns all device memory and gives none out at execution
+ * time, or in a serving loop with a fixed memory budget where cudaMalloc
+ * could block on the device or fail under fragmentation.  This entry point
+ * takes the same arguments as verify_attn_e4m3_ex without the workspace:
+ * the FP32 partials and the status word live in a fixed scratch array of
+ * VAE4_NOALLOC_SCRATCH_BYTES (8 MiB) that the library declares statically,
+ * so every GPU that loads the library keeps those 8 MiB reserved until the
+ * process exits.  Nothing is allocated or freed: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ *  - The first call on a device looks up the scratch array's device
+ *    address (once per device, with that device current).  Make that first
+ *    call before any stream capture on the device.
+ *  - A call whose partition plan needs more than VAE4_NOALLOC_SCRATCH_BYTES
+ *    (see verify_attn_e4m3_workspace_bytes) returns VAE4_ERR_WORKSPACE and
+ *    launches nothing.  Example sizes: the 262144-token q8 GQA6 D256 step
+ *    on 152 SMs needs about 7.2 MiB.
+ *  - Every call on a device shares the one scratch array and leaves its
+ *    contents behind.  Nothing in it has to start at zero (each call writes
+ *    every partial it reads), so no clearing is done.  Calls whose kernels
+ *    overlap on the GPU (different streams without ordering) race on the
+ *    scratch and give wrong results: order them.
+ *  - Device-side data errors zero the affected sequence's output exactly as
+ *    in verify_attn_e4m3_ex; the status word is not readable from here.
+ * Returns VAE4_OK or a negative vae4_error.
+ */
+int verify_attn_e4m3_noalloc(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                             const vae4_tensor *block_table,
+                             const vae4_tensor *seq_lens,
+                             const vae4_tensor *kv_scales, const vae4_tensor *out,
+                             vae4_stream stream, const vae4_options *opt);
+
 #ifdef __cplusplus
 }
 #endif
