@@ -16,6 +16,8 @@ ABI_VERSION = 1
 
 VAE4_U8, VAE4_I32, VAE4_F16, VAE4_F32 = 1, 2, 3, 4
 
+FLAG_WARP_MMA = 0x1
+
 STATUS_BAD_BLOCK = 0x1
 STATUS_BAD_LENGTH = 0x2
 STATUS_BAD_QLEN = 0x4
@@ -108,7 +110,7 @@ def load(build_if_stale: bool = True):
         lib.verify_attn_e4m3_clear_status.restype = ctypes.c_int
         lib.verify_attn_e4m3_decode_table.argtypes = [ctypes.c_void_p,
                                                       ctypes.POINTER(ctypes.c_int32),
-                                                      ctypes.c_void_p]
+                                                      ctypes.c_int32, ctypes.c_void_p]
         lib.verify_attn_e4m3_decode_table.restype = ctypes.c_int
         lib.verify_attn_e4m3_noalloc.argtypes = [P] * 6 + [ctypes.c_void_p,
                                                            ctypes.POINTER(Options)]
@@ -173,13 +175,13 @@ def _check(rc: int, where: str):
 # ----------------------------------------------------------------------------
 def verify_attn_e4m3(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, *,
                      softmax_scale: float = 0.0, partition_tokens: int = 0,
-                     max_seq_len: int = 0, num_sms: int = 0, stream=None):
+                     max_seq_len: int = 0, num_sms: int = 0, flags: int = 0, stream=None):
     """Run the verify step into ``out``.  All tensors on the current device;
     see include/verify_attn_e4m3.h for layouts.  Asynchronous on ``stream``
     (torch's current stream by default)."""
     lib = load()
     opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
-                  int(num_sms), 0)
+                  int(num_sms), int(flags))
     descs = [describe(t) for t in (q, kv_pages, block_table, seq_lens, kv_scales, out,
                                    workspace)]
     rc = lib.verify_attn_e4m3_ex(*[ctypes.byref(x) for x in descs],
@@ -192,10 +194,11 @@ verify = verify_attn_e4m3
 
 
 def _stage(name, q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, *,
-           softmax_scale=0.0, partition_tokens=0, max_seq_len=0, num_sms=0, stream=None):
+           softmax_scale=0.0, partition_tokens=0, max_seq_len=0, num_sms=0, flags=0,
+           stream=None):
     lib = load()
     opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
-                  int(num_sms), 0)
+                  int(num_sms), int(flags))
     descs = [describe(t) for t in (q, kv_pages, block_table, seq_lens, kv_scales, out,
                                    workspace)]
     rc = getattr(lib, name)(*[ctypes.byref(x) for x in descs],
@@ -287,14 +290,15 @@ def verify_attn_e4m3_clear_status(workspace, stream=None):
 clear_status = verify_attn_e4m3_clear_status
 
 
-def verify_attn_e4m3_decode_table(stream=None):
+def verify_attn_e4m3_decode_table(flags: int = 0, stream=None):
     """(fp16 bit patterns of the 256 decoded codes as a device uint16-in-int16
-    tensor, scale exponent): code b decodes to dec(b) * 2^scale_log2."""
+    tensor, scale exponent): code b decodes to dec(b) * 2^scale_log2.  flags
+    picks the kernel whose decoder runs (0 = tcgen05 path)."""
     import torch
     out = torch.empty(256, dtype=torch.int16, device="cuda")
     e = ctypes.c_int32(0)
     _check(load().verify_attn_e4m3_decode_table(ctypes.c_void_p(out.data_ptr()),
-                                                ctypes.byref(e),
+                                                ctypes.byref(e), int(flags),
                                                 ctypes.c_void_p(_stream_handle(stream))),
            "decode_table")
     return out, e.value

@@ -24,6 +24,14 @@ constexpr int64_t kMaxPartitions = 8192;  // per (sequence, KV head)
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+// Rows of FP32 partial state per (sequence, KV head, partition): enough for
+// both split kernels' row layouts.
+int64_t ws_rows(int rows) {
+  int n_rg = 1, n = 16;
+  vae4::tc_row_groups(rows, &n_rg, &n);
+  return std::max<int64_t>(align_up(rows, 16), (int64_t)n_rg * n);
+}
+
 struct WsLayout {
   int64_t ml_off, o_off, total;
 };
@@ -92,7 +100,17 @@ struct Prepared {
   CombineParams cp;
   int64_t ws_needed;
   bool empty;
+  bool warp_mma;
 };
+
+// SM cycles a pipeline wait of the tcgen05 kernel may take before the CTA
+// gives up (about a second at the GB300 clock).
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+cudaError_t launch_split(const Prepared &pr, cudaStream_t st) {
+  return pr.warp_mma ? vae4::launch_split_mma(pr.sp, st)
+                     : vae4::launch_split_tc(pr.sp, kWaitLimitCycles, st);
+}
 
 int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
             const vae4_tensor *seq, const vae4_tensor *sc, const vae4_tensor *out,
@@ -101,7 +119,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   vae4_options o;
   memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
-  if (o.flags != 0) return VAE4_ERR_OPTIONS;
+  if ((o.flags & ~VAE4_FLAG_WARP_MMA) != 0) return VAE4_ERR_OPTIONS;
 
   int rc = check_qo(q);
   if (rc) return rc;
@@ -124,11 +142,13 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
       kv->stride[1] != Hkv * page * D || kv->stride[0] != 2 * Hkv * page * D)
     return VAE4_ERR_STRIDE;
   if (!al16(kv->data)) return VAE4_ERR_MISALIGNED;
+  // the pool is addressed as rows of D bytes by 32-bit TMA coordinates
+  if (n_pages * 2 * Hkv * page > (int64_t)0x7fffff00) return VAE4_ERR_SHAPE;
   if (Hq % Hkv != 0) return VAE4_ERR_GQA;
   const int64_t G = Hq / Hkv;
   const int64_t rows = Qmax * G;
-  const int64_t rows_pad = align_up(rows, 16);
-  if (rows_pad > kMaxRowsPad) return VAE4_ERR_UNSUPPORTED;
+  if (align_up(rows, 16) > kMaxRowsPad) return VAE4_ERR_UNSUPPORTED;
+  const int64_t rows_pad = ws_rows((int)rows);
 
   // block table: I32 [B][max_pages]
   if (bt->dtype != VAE4_I32) return VAE4_ERR_DTYPE;
@@ -178,6 +198,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   const WsLayout lay = ws_layout((int)B, (int)Hkv, P, (int)rows_pad, (int)D);
   pr->ws_needed = lay.total;
   pr->empty = (B == 0);
+  pr->warp_mma = (o.flags & VAE4_FLAG_WARP_MMA) != 0;
   if (B > 0 && ws->shape[0] < lay.total) return VAE4_ERR_WORKSPACE;
   if (!q->data || !kv->data || !bt->data || !seq->data || !sc->data || !out->data ||
       !ws->data) {
@@ -264,7 +285,7 @@ int verify_attn_e4m3_ex(const vae4_tensor *q, const vae4_tensor *kv_pages,
   if (rc) return rc;
   if (pr.empty) return VAE4_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (vae4::launch_split_mma(pr.sp, st) != cudaSuccess) return VAE4_ERR_CUDA;
+  if (launch_split(pr, st) != cudaSuccess) return VAE4_ERR_CUDA;
   if (vae4::launch_combine(pr.cp, st) != cudaSuccess) return VAE4_ERR_CUDA;
   return VAE4_OK;
 }
@@ -278,7 +299,7 @@ int verify_attn_e4m3_partials(const vae4_tensor *q, const vae4_tensor *kv_pages,
   int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
   if (rc) return rc;
   if (pr.empty) return VAE4_OK;
-  if (vae4::launch_split_mma(pr.sp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (launch_split(pr, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VAE4_ERR_CUDA;
   return VAE4_OK;
 }
@@ -322,8 +343,8 @@ int64_t verify_attn_e4m3_workspace_bytes(int B, int Hq, int Hkv, int Qmax, int D
     return VAE4_ERR_SHAPE;
   if (D != 64 && D != 128 && D != 256) return VAE4_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return VAE4_ERR_GQA;
-  const int64_t rows_pad = align_up((int64_t)Qmax * (Hq / Hkv), 16);
-  if (rows_pad > kMaxRowsPad) return VAE4_ERR_UNSUPPORTED;
+  if (align_up((int64_t)Qmax * (Hq / Hkv), 16) > kMaxRowsPad) return VAE4_ERR_UNSUPPORTED;
+  const int64_t rows_pad = ws_rows(Qmax * (Hq / Hkv));
   int sms = num_sms;
   if (sms < 0) return VAE4_ERR_SHAPE;
   if (sms == 0) {
@@ -377,11 +398,14 @@ int verify_attn_e4m3_clear_status(const vae4_tensor *workspace, vae4_stream stre
   return VAE4_OK;
 }
 
-int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2, vae4_stream stream) {
+int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2, int32_t flags,
+                                  vae4_stream stream) {
   if (!dev_out || !scale_log2) return VAE4_ERR_NULL;
   if (!al16(dev_out)) return VAE4_ERR_MISALIGNED;
-  *scale_log2 = -8;
-  if (vae4::launch_decode_table(static_cast<uint16_t *>(dev_out),
+  if ((flags & ~VAE4_FLAG_WARP_MMA) != 0) return VAE4_ERR_OPTIONS;
+  const bool integer_path = (flags & VAE4_FLAG_WARP_MMA) != 0;
+  *scale_log2 = integer_path ? -8 : 0;
+  if (vae4::launch_decode_table(static_cast<uint16_t *>(dev_out), integer_path,
                                 reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VAE4_ERR_CUDA;
   return VAE4_OK;

@@ -126,12 +126,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   *reinterpret_cast<uint2 *>(out + 4 * l4) = res;
 }
 
-__global__ void decode_table_kernel(uint16_t *out) {
+__global__ void decode_table_kernel(uint16_t *out, bool integer_path) {
   const int t = threadIdx.x;  // 64 threads x 4 codes
   const uint32_t w = (uint32_t)(4 * t) | (uint32_t)(4 * t + 1) << 8 | (uint32_t)(4 * t + 2) << 16 |
                      (uint32_t)(4 * t + 3) << 24;
   uint32_t lo, hi;
-  e4m3x4_to_f16x4(w, lo, hi);
+  if (integer_path)
+    e4m3x4_to_f16x4(w, lo, hi);
+  else
+    e4m3x4_to_f16x4_hw(w, lo, hi);
   out[4 * t + 0] = (uint16_t)(lo & 0xFFFFu);
   out[4 * t + 1] = (uint16_t)(lo >> 16);
   out[4 * t + 2] = (uint16_t)(hi & 0xFFFFu);
@@ -167,8 +170,8 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
   }
 }
 
-cudaError_t launch_decode_table(uint16_t *out, cudaStream_t stream) {
-  decode_table_kernel<<<1, 64, 0, stream>>>(out);
+cudaError_t launch_decode_table(uint16_t *out, bool integer_path, cudaStream_t stream) {
+  decode_table_kernel<<<1, 64, 0, stream>>>(out, integer_path);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,27 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo,
   hi = t1 - ((t1 >> 1) & 0x3F803F80u);
 }
 
+// Hardware converter: two E4M3 bytes -> f16x2, exact for every finite code
+// (every E4M3 value is an FP16 value); byte 0 -> low half.  The two NaN
+// codes become FP16 NaN.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint32_t two_bytes) {
+  uint32_t d;
+  const unsigned short v = (unsigned short)(two_bytes & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(d) : "h"(v));
+  return d;
+}
+// Four E4M3 bytes -> two f16x2 words (lo = bytes 0,1; hi = bytes 2,3), dec(b).
+__device__ __forceinline__ void e4m3x4_to_f16x4_hw(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  lo = cvt_e4m3x2(w);
+  hi = cvt_e4m3x2(w >> 16);
+}
+__device__ __forceinline__ void e4m3x16_to_f16x16_hw(const uint4 &raw, uint4 &h0, uint4 &h1) {
+  e4m3x4_to_f16x4_hw(raw.x, h0.x, h0.y);
+  e4m3x4_to_f16x4_hw(raw.y, h0.z, h0.w);
+  e4m3x4_to_f16x4_hw(raw.z, h1.x, h1.y);
+  e4m3x4_to_f16x4_hw(raw.w, h1.z, h1.w);
+}
+
 // 16 bytes -> 16 halves (two uint4 of f16x2).
 __device__ __forceinline__ void e4m3x16_to_f16x16(const uint4 &raw, uint4 &h0,
                                                   uint4 &h1) {

@@ -14,10 +14,17 @@ size_t split_mma_smem_bytes(int D, int rows_pad);
 int split_mma_threads(int rows_pad);
 cudaError_t launch_split_mma(const SplitParams &p, cudaStream_t stream);
 
+// Split kernel on the tcgen05 tensor cores (TMA + TMEM); the default path.
+// wait_limit: SM cycles after which a pipeline wait gives up.
+cudaError_t launch_split_tc(const SplitParams &p, long long wait_limit, cudaStream_t stream);
+// Row groups of the tcgen05 kernel: rows are processed in n_rg groups of n
+// (a multiple of 16, at most 64) rows; the workspace needs n_rg * n rows.
+void tc_row_groups(int rows, int *n_rg, int *n);
+
 // Combine kernel (programmatic dependent launch after the split kernel).
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 
 // Decode-table test hook.
-cudaError_t launch_decode_table(uint16_t *out, cudaStream_t stream);
+cudaError_t launch_decode_table(uint16_t *out, bool integer_path, cudaStream_t stream);
 
 }  // namespace vae4

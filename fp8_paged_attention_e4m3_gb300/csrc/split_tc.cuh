@@ -1,0 +1,603 @@
+// Split (partition) kernel on the 5th-generation tensor cores (tcgen05, TMEM
+// accumulators, TMA tensor loads) -- the production path on sm_103a.
+//
+// One CTA = one (partition p, KV head h and row group, sequence b).  The
+// context is walked in 128-key tiles made of two 64-key half-tiles.
+// Warp roles (20 warps):
+//
+//   K / V producer  : one thread each walks the block table and issues TMA
+//                     tensor loads (128-byte swizzle) of the E4M3 K (resp. V)
+//                     page slices of a half-tile into its own ring (K: 2
+//                     slots, V: 2 or 3).  Keys past the partition and pages
+//                     with invalid ids are loaded from outside the tensor,
+//                     which fills zeros.
+//   K decoders (4)  : thread = key; exact E4M3 -> FP16 with the hardware
+//                     converter, straight into tensor memory: the A operand
+//                     of S^T = K . Q^T (lane = key, column = pair of d).
+//   V decoders (4)  : thread = key; same decode into a 3-slot ring of FP16
+//                     V^T half-tiles in shared memory (MN-major, 128-byte
+//                     swizzle), so V is decoded as soon as it lands.
+//   score MMA warp  : issues tcgen05.mma.kind::f16  S^T[128 x N] = K . Q^T
+//   value MMA warp  : issues tcgen05.mma.kind::f16  O^T[d x N] += V^T . P^T
+//                     (FP32 accumulators in TMEM; commits to mbarriers).
+//   softmax (8)     : thread = key, half of the N rows each; loads S^T from
+//                     TMEM, applies the causal / partition mask at the
+//                     edges, keeps the FP32 running max per row (raised
+//                     lazily: only when a score exceeds it by more than 2^8,
+//                     then running sums and TMEM O^T columns are rescaled),
+//                     writes P = 2^(t - m) as FP16 and adds the same rounded
+//                     P into FP32 per-row sums.
+//
+// Rows are (query i, group head g) pairs r = i*G + g of KV head h; N of them
+// (<= 64) per CTA form the N dimension of both products (48 for q8 GQA6).
+// The partition's FP32 (max, sum, unnormalised P.V) go to the workspace for
+// the combine kernel ("FP32 max/sum and unnormalized PV until the final
+// combine", PR #524 "[Kernel][SM70] Add opt-in E4M3 grouped attention with
+// FP32 partials", final status).  Keys are visited in ascending logical
+// order, so the result does not depend on where pages live.
+//
+// Every mbarrier wait is bounded; on expiry the CTA raises an abort flag,
+// every role winds down, outstanding copies and MMAs are drained, TMEM is
+// freed and the partition is marked invalid (sum = -1, status TIMEOUT).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "params.h"
+#include "tc_ptx.cuh"
+#include "verify_attn_e4m3.h"
+
+namespace vae4 {
+
+struct TcArgs {
+  int64_t rows_total;    // rows of D bytes in the pool view of the tensor map
+  long long wait_limit;  // SM cycles before a wait gives up
+  int32_t n_rg;          // row groups per KV head
+};
+
+template <int D, int N>
+struct TcCfg {
+  static_assert(N % 16 == 0 && N >= 16 && N <= 64, "rows per CTA");
+  static constexpr int NSW = 8;                 // softmax warps
+  static constexpr int NC = N / 2;              // rows per softmax thread
+  static constexpr int IB = D < 128 ? D : 128;  // TMA box inner bytes
+  static constexpr int NDH = D / IB;            // boxes per key row
+  static constexpr int SMASK = IB == 128 ? 7 : 3;     // 128B / 64B swizzle
+  static constexpr int DB = D / 64 < 2 ? 2 : D / 64;  // 64-d blocks of V^T (D=64 padded)
+  static constexpr int MH = DB / 2;             // 128-row M halves of V^T.P^T
+  static constexpr int SC = (N + 31) / 32 * 32; // TMEM columns per accumulator
+  static constexpr int KCOL = 0, SCOL = 128, OCOL = 128 + 2 * SC;
+  static constexpr int NKR = 2;                 // K raw slots (>= 2)
+  static constexpr int QB = (D / 64) * N * 128; // Q, K-major SW128
+  static constexpr int VSLOT = DB * 64 * 128;   // one FP16 V^T half-tile
+  static constexpr int PB = 128 * 128;          // P^T, MN-major SW128 (N <= 64)
+  static constexpr int RSLOT = 64 * D;          // one raw K or V half-tile
+  static constexpr int SMALL = 2688;
+  static constexpr int LIMIT = 232448 - 1024;   // opt-in maximum minus alignment slack
+  // FP16 V^T slots and V raw slots (NVR >= NVF keeps the decoders' slot
+  // waits unambiguous): 3 and 3 when they fit, else 2 and 2
+  static constexpr bool FIT3 = QB + 3 * VSLOT + PB + (NKR + 3) * RSLOT + SMALL <= LIMIT;
+  static constexpr int NVF = FIT3 ? 3 : 2;
+  static constexpr int NVR = FIT3 ? 3 : 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_V = OFF_Q + QB;
+  static constexpr int OFF_P = OFF_V + NVF * VSLOT;
+  static constexpr int OFF_KR = OFF_P + PB;
+  static constexpr int OFF_VR = OFF_KR + NKR * RSLOT;
+  static constexpr int OFF_SMALL = OFF_VR + NVR * RSLOT;
+  static constexpr int SMEM = OFF_SMALL + SMALL + 1024;
+  static constexpr int NTHREADS = 32 * 20;
+  // mbarrier indices, derived from the ring sizes so no two roles share one
+  static constexpr int B_KFULL = 0, B_KEMPTY = B_KFULL + NKR, B_VFULL = B_KEMPTY + NKR,
+                       B_VEMPTY = B_VFULL + NVR, B_KREADY = B_VEMPTY + NVR,
+                       B_KFREE = B_KREADY + 1, B_VREADY = B_KFREE + 1, B_VFREE = B_VREADY + NVF,
+                       B_SFULL = B_VFREE + NVF, B_SFREE = B_SFULL + 2, B_PREADY = B_SFREE + 2,
+                       B_PVDONE = B_PREADY + 1, B_DRAINQK = B_PVDONE + 1,
+                       B_DRAINPV = B_DRAINQK + 1, NBARS = B_DRAINPV + 1;
+  static_assert(NBARS * 8 <= 320, "barriers fit below the small-region scalars");
+  static_assert(NKR <= 4 && NVR <= 4, "producer bookkeeping");
+  static_assert(NKR >= 2 && NVR >= NVF, "slot reuse order (see the decoders)");
+  static_assert(OCOL + MH * SC <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NC % 8 == 0, "softmax column groups of 8");
+};
+
+// warp roles
+enum : int {
+  kWSoftmax = 0,   // 0..7
+  kWKDec = 8,      // 8..11 (quadrant = warp & 3)
+  kWVDec = 12,     // 12..15
+  kWKProd = 16, kWVProd = 17, kWQk = 18, kWPv = 19
+};
+// offsets in the small region (the mbarriers occupy its first 320 bytes)
+constexpr int kSmTslot = 320, kSmAbort = 324, kSmBad = 328, kSmVotes = 352, kSmM = 384,
+              kSmPos = 640, kSmMNew = 896, kSmBase = 1152, kSmThr = 1408,
+              kSmRed = 1664;  // red: 8 warps x 32 floats
+
+__device__ __forceinline__ uint32_t sw128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+
+template <int D, int N>
+__global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
+    split_tc_kernel(const SplitParams p, const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
+  using C = TcCfg<D, N>;
+  constexpr int kKFull = C::B_KFULL, kKEmpty = C::B_KEMPTY, kVFull = C::B_VFULL,
+                kVEmpty = C::B_VEMPTY, kKReady = C::B_KREADY, kKFree = C::B_KFREE,
+                kVReady = C::B_VREADY, kVFree = C::B_VFREE, kSFull = C::B_SFULL,
+                kSFree = C::B_SFREE, kPReady = C::B_PREADY, kPvDone = C::B_PVDONE,
+                kDrainQk = C::B_DRAINQK, kDrainPv = C::B_DRAINPV;
+  extern __shared__ uint8_t smem_raw[];
+  const float kInf = __int_as_float(0x7f800000);
+  constexpr float kLog2e = 1.4426950408889634f;
+  constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units)
+
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (sbase - raw_addr);
+  const uint32_t sQ = sbase + C::OFF_Q, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P,
+                 sKR = sbase + C::OFF_KR, sVR = sbase + C::OFF_VR, sSm = sbase + C::OFF_SMALL;
+  uint8_t *gQ = gbase + C::OFF_Q, *gV = gbase + C::OFF_V, *gP = gbase + C::OFF_P,
+          *gKR = gbase + C::OFF_KR, *gVR = gbase + C::OFF_VR, *gSm = gbase + C::OFF_SMALL;
+  auto bar = [&](int i) -> uint32_t { return sSm + 8u * (uint32_t)i; };
+  volatile int *abort_f = reinterpret_cast<volatile int *>(gSm + kSmAbort);
+  volatile int *bad_f = reinterpret_cast<volatile int *>(gSm + kSmBad);
+  volatile int *votes = reinterpret_cast<volatile int *>(gSm + kSmVotes);
+  float *m_s = reinterpret_cast<float *>(gSm + kSmM);      // running max (log2 units)
+  int *pos_s = reinterpret_cast<int *>(gSm + kSmPos);      // last visible key per row
+  float *mnew_s = reinterpret_cast<float *>(gSm + kSmMNew);
+  float *base_s = reinterpret_cast<float *>(gSm + kSmBase);  // m, or 0 while m = -inf
+  float *thr_s = reinterpret_cast<float *>(gSm + kSmThr);    // (m + tau) / alpha
+  float *red = reinterpret_cast<float *>(gSm + kSmRed);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int part = blockIdx.x, b = blockIdx.z;
+  const int h = blockIdx.y / a.n_rg, rg = blockIdx.y - h * a.n_rg;
+  const int row0 = rg * N;  // first row of this CTA's row group
+
+  // ---- sequence, partition
+  const int L = p.seq[(int64_t)b * p.seq_sb];
+  const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
+  if (L < 0 || L > p.capacity) {
+    if (part == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, VAE4_STATUS_BAD_LENGTH);
+    return;
+  }
+  if (ql < 0 || ql > p.Qmax || (L > 0 && ql > L)) {
+    if (part == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
+    return;
+  }
+  const int k0 = part * p.T;
+  if (k0 >= L) return;  // dead partition
+  const int k1 = min(k0 + p.T, L);
+  const int ntiles = (k1 - k0 + 127) >> 7;
+  const int nhalf = 2 * ntiles;  // half-tiles, the last may be all padding
+
+  // ---- set-up: barriers, queries, per-row state, TMEM
+  if (tid == 0) {
+    // arrival counts: TMA (expect_tx) and MMA commits arrive once; a K or V
+    // half-tile is consumed by 2 decoder warps; K for a tile comes from 4.
+    for (int i = 0; i < C::NBARS; ++i) {
+      uint32_t cnt = 1;
+      if ((i >= kKEmpty && i < kKEmpty + C::NKR) || (i >= kVEmpty && i < kVEmpty + C::NVR) ||
+          (i >= kVReady && i < kVReady + C::NVF))
+        cnt = 64;
+      else if (i == kKReady)
+        cnt = 128;
+      else if ((i >= kSFree && i < kSFree + 2) || i == kPReady)
+        cnt = 32 * C::NSW;
+      tc::mbar_init(bar(i), cnt);
+    }
+    *abort_f = 0;
+    *bad_f = 0;
+  }
+  {
+    const __half *qb = static_cast<const __half *>(p.q) + (int64_t)b * p.q_sb;
+    constexpr int QCH = D / 8;  // 16-byte chunks per query row
+    for (int c = tid; c < N * QCH; c += C::NTHREADS) {
+      const int r = c / QCH, cc = c - r * QCH;
+      const int rr = row0 + r, i = rr / p.G, g = rr - i * p.G;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (rr < p.rows && i < ql)
+        v = __ldg(reinterpret_cast<const uint4 *>(qb + (int64_t)i * p.q_si +
+                                                  (int64_t)(h * p.G + g) * p.q_sh + cc * 8));
+      const int katom = cc >> 3, c8 = cc & 7;
+      *reinterpret_cast<uint4 *>(gQ + katom * (N * 128) + sw128(r * 128 + c8 * 16)) = v;
+    }
+    for (int r = tid; r < N; r += C::NTHREADS) {
+      const int rr = row0 + r, i = rr / p.G;
+      pos_s[r] = (rr < p.rows && i < ql) ? L - ql + i : -1;
+      m_s[r] = -kInf;
+      base_s[r] = 0.f;
+      thr_s[r] = -kInf;
+    }
+    if (D == 64) {  // the padding 64-d block of every V^T slot reads as zeros
+      for (int c = tid; c < C::NVF * 512; c += C::NTHREADS) {
+        const int s = c >> 9, rem = c & 511;
+        *reinterpret_cast<uint4 *>(gV + s * C::VSLOT + 8192 + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+  if (warp == kWQk) {
+    tc::tmem_alloc(sSm + kSmTslot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_proxy_async_smem();
+  tc::mbar_fence_init();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(gSm + kSmTslot);
+  const long long LIM = a.wait_limit;
+
+  int issued[4] = {0, 0, 0, 0};  // producers: uses issued per ring slot
+  bool mma_issued = false;    // this thread issued tcgen05.mma
+
+  if (warp == kWKProd || warp == kWVProd) {
+    // =============================== producers (K ring, V ring)
+    if (lane == 0) {
+      const bool isv = warp == kWVProd;
+      const int nslot = isv ? C::NVR : C::NKR;
+      const int fullb = isv ? kVFull : kKFull, emptyb = isv ? kVEmpty : kKEmpty;
+      const uint32_t ring = isv ? sVR : sKR;
+      tc::prefetch_tensormap(&tmap);
+      const int page_shift = __ffs(p.page) - 1;
+      for (int t = 0; t < nhalf; ++t) {
+        const int st = t % nslot, u = t / nslot;
+        if (t >= nslot && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
+        tc::mbar_arrive_expect_tx(bar(fullb + st), C::RSLOT);
+        issued[st] = u + 1;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int key0 = k0 + 64 * t + 16 * g;
+          int row = (int)a.rows_total;  // outside the tensor: zero fill
+          if (key0 < k1) {
+            const int lp = key0 >> page_shift;
+            const int phys = p.bt[(int64_t)b * p.bt_sb + lp];
+            if (phys >= 0 && phys < p.n_pages)
+              row = (int)(((int64_t)phys * 2 * p.Hkv + (isv ? p.Hkv : 0) + h) * p.page +
+                          (key0 - (lp << page_shift)));
+            else
+              *bad_f = 1;
+          }
+#pragma unroll
+          for (int dh = 0; dh < C::NDH; ++dh)
+            tc::tma_load_2d(ring + st * C::RSLOT + dh * (64 * C::IB) + g * (16 * C::IB), &tmap,
+                            dh * C::IB, row, bar(fullb + st));
+        }
+      }
+    }
+  } else if (warp == kWQk) {
+    // =============================== score MMA issuer: S^T = K . Q^T
+    if (lane == 0) {
+      constexpr uint32_t id_qk = tc::idesc_f16(128, N, 0, 0);
+      for (int j = 0; j < ntiles; ++j) {
+        if (!tc::mbar_wait(bar(kKReady), j & 1, abort_f, LIM)) break;
+        if (j >= 2 && !tc::mbar_wait(bar(kSFree + (j & 1)), ((j >> 1) - 1) & 1, abort_f, LIM))
+          break;
+        tc::tc_fence_after();
+        const uint32_t d = tbase + C::SCOL + (j & 1) * C::SC;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t bq = sQ + (ks >> 2) * (N * 128) + (ks & 3) * 32;
+          tc::mma_ts(d, tbase + C::KCOL + ks * 8, tc::smem_desc(bq, 16, 1024), id_qk, ks > 0);
+        }
+        tc::mma_commit(bar(kSFull + (j & 1)));
+        tc::mma_commit(bar(kKFree));
+        mma_issued = true;
+      }
+    }
+  } else if (warp == kWPv) {
+    // =============================== value MMA issuer: O^T += V^T . P^T
+    if (lane == 0) {
+      constexpr uint32_t id_pv = tc::idesc_f16(128, N, 1, 1);
+      bool ok = true;
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (!(ok = tc::mbar_wait(bar(kPReady), j & 1, abort_f, LIM))) break;
+        for (int kh = 0; kh < 2 && ok; ++kh) {
+          const int t = 2 * j + kh, vs = t % C::NVF;
+          if (!(ok = tc::mbar_wait(bar(kVReady + vs), (t / C::NVF) & 1, abort_f, LIM))) break;
+          tc::tc_fence_after();
+#pragma unroll
+          for (int mh = 0; mh < C::MH; ++mh) {
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int ks = kh * 4 + k4;
+              const uint32_t av = sV + vs * C::VSLOT + (2 * mh) * 8192 + k4 * 2048;
+              const uint32_t bp = sP + ks * 2048;
+              tc::mma_ss(tbase + C::OCOL + mh * C::SC, tc::smem_desc(av, 8192, 1024),
+                         tc::smem_desc(bp, 16384, 1024), id_pv, (j > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          tc::mma_commit(bar(kVFree + vs));
+          mma_issued = true;
+        }
+        if (!ok) break;
+        tc::mma_commit(bar(kPvDone));
+      }
+    }
+  } else if (warp >= kWKDec) {
+    // =============================== decoders (thread = key)
+    const bool isv = warp >= kWVDec;
+    const int dq = warp & 3;              // TMEM lane quadrant = keys 32*dq.. of a tile
+    const int kh = dq >> 1;               // half-tile of the 128-key tile
+    const int kk = 32 * (dq & 1) + lane;  // key within the half-tile
+    const uint32_t lane_off = (uint32_t)(32 * dq) << 16;
+    for (int j = 0; j < ntiles; ++j) {
+      const int t = 2 * j + kh;
+      if (!isv) {
+        // K -> TMEM: column c holds d = 2c (low half), 2c+1 (high half).
+        // Wait for the previous tile's score MMA first: it proves every
+        // earlier K half-tile (in particular this slot's previous use, t -
+        // NKR <= t - 2) has landed and been read, so the parity wait on the
+        // slot below cannot match an older phase when pairs share slots.
+        const int st = t % C::NKR;
+        if (j > 0 && !tc::mbar_wait(bar(kKFree), (j - 1) & 1, abort_f, LIM)) break;
+        if (!tc::mbar_wait(bar(kKFull + st), (t / C::NKR) & 1, abort_f, LIM)) break;
+        tc::tc_fence_after();
+        const uint8_t *rawK = gKR + st * C::RSLOT;
+#pragma unroll
+        for (int grp = 0; grp < D / 64; ++grp) {
+          uint32_t r[32];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int c = grp * 4 + q4;  // 16-byte chunk of the key row
+            const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
+            const uint32_t off = (uint32_t)(kk * C::IB + cc * 16);
+            const uint4 w = *reinterpret_cast<const uint4 *>(
+                rawK + dh * (64 * C::IB) + (off ^ (((off >> 7) & C::SMASK) << 4)));
+            e4m3x4_to_f16x4_hw(w.x, r[q4 * 8 + 0], r[q4 * 8 + 1]);
+            e4m3x4_to_f16x4_hw(w.y, r[q4 * 8 + 2], r[q4 * 8 + 3]);
+            e4m3x4_to_f16x4_hw(w.z, r[q4 * 8 + 4], r[q4 * 8 + 5]);
+            e4m3x4_to_f16x4_hw(w.w, r[q4 * 8 + 6], r[q4 * 8 + 7]);
+          }
+          const uint32_t (&r0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[0]);
+          const uint32_t (&r1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[16]);
+          tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32, r0);
+          tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32 + 16, r1);
+        }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(bar(kKReady));
+        tc::mbar_arrive(bar(kKEmpty + st));
+      } else {
+        // V -> FP16 V^T slot (MN-major, 128-byte swizzle).  Wait for the
+        // value MMA that last read the FP16 slot first: it proves half-tiles
+        // up to t - NVF >= t - NVR were decoded, i.e. this raw slot's
+        // previous use is complete, so the parity wait below is unambiguous.
+        const int st = t % C::NVR, vs = t % C::NVF;
+        if (t >= C::NVF && !tc::mbar_wait(bar(kVFree + vs), ((t / C::NVF) - 1) & 1, abort_f, LIM))
+          break;
+        if (!tc::mbar_wait(bar(kVFull + st), (t / C::NVR) & 1, abort_f, LIM)) break;
+        const uint8_t *rawV = gVR + st * C::RSLOT;
+        uint8_t *vdst = gV + vs * C::VSLOT;
+#pragma unroll 4
+        for (int c = 0; c < D / 16; ++c) {
+          const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
+          const uint32_t off = (uint32_t)(kk * C::IB + cc * 16);
+          const uint4 w = *reinterpret_cast<const uint4 *>(
+              rawV + dh * (64 * C::IB) + (off ^ (((off >> 7) & C::SMASK) << 4)));
+          uint4 h0, h1;
+          e4m3x16_to_f16x16_hw(w, h0, h1);
+          const int dblk = c >> 2, c2 = 2 * (c & 3);
+          uint8_t *blk = vdst + dblk * 8192;
+          *reinterpret_cast<uint4 *>(blk + sw128((uint32_t)(kk * 128 + c2 * 16))) = h0;
+          *reinterpret_cast<uint4 *>(blk + sw128((uint32_t)(kk * 128 + (c2 + 1) * 16))) = h1;
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(bar(kVReady + vs));
+        tc::mbar_arrive(bar(kVEmpty + st));
+      }
+    }
+  } else {
+    // =============================== softmax (thread = key, NC rows)
+    const int q = warp & 3, cg = warp >> 2;
+    const int col0 = cg * C::NC;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    // K holds dec(b) exactly; t = S * alpha is the score in log2 units
+    const float alpha = p.sm_scale * p.scales[h * p.scale_sh] * kLog2e;
+    // every real row sees keys 0 .. L - q_len; padding rows have zero
+    // queries (finite, never output), so only tiles past that key or past
+    // the partition end need the per-row mask
+    const int min_pos = L - ql;
+    constexpr int nsm = 32 * C::NSW;
+    float lpart[C::NC];
+#pragma unroll
+    for (int c = 0; c < C::NC; ++c) lpart[c] = 0.f;
+    bool alive = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int buf = j & 1;
+      float s[C::NC];
+      alive = alive && tc::mbar_wait(bar(kSFull + buf), (j >> 1) & 1, abort_f, LIM);
+      if (alive) {
+        tc::tc_fence_after();
+#pragma unroll
+        for (int c8 = 0; c8 < C::NC / 8; ++c8) {
+          uint32_t r[8];
+          tc::tmem_ld8(tbase + lane_off + C::SCOL + buf * C::SC + col0 + c8 * 8, r);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s[c8 * 8 + e] = __uint_as_float(r[e]);
+        }
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::NC; ++c) s[c] = 0.f;
+      }
+      tc::mbar_arrive(bar(kSFree + buf));
+
+      const int key = k0 + 128 * j + 32 * q + lane;
+      bool exceed = false;
+      if (key < k1 && key <= min_pos) {
+#pragma unroll
+        for (int c = 0; c < C::NC; ++c) exceed |= s[c] > thr_s[col0 + c];
+      } else {
+        const bool kvalid = key < k1;
+#pragma unroll
+        for (int c = 0; c < C::NC; ++c) {
+          s[c] = (kvalid && key <= pos_s[col0 + c]) ? s[c] : -kInf;
+          exceed |= s[c] > thr_s[col0 + c];
+        }
+      }
+      exceed = __any_sync(0xffffffffu, exceed);
+      if (lane == 0) votes[warp] = exceed ? 1 : 0;
+      tc::named_bar(1, nsm);
+      bool any = false;
+#pragma unroll
+      for (int w = 0; w < C::NSW; ++w) any |= votes[w] != 0;
+      tc::named_bar(1, nsm);  // votes read before the next tile rewrites them
+      if (any) {
+        // exact tile maximum per row over the 128 keys (4 quadrant warps)
+#pragma unroll
+        for (int c = 0; c < C::NC; ++c) {
+          float mx = s[c];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (lane == 0) red[warp * 32 + c] = mx * alpha;  // -inf stays -inf
+        }
+        tc::named_bar(1, nsm);
+        if (q == 0 && lane < C::NC) {  // one warp per column group combines the quadrants
+          float mt = red[(cg * 4) * 32 + lane];
+#pragma unroll
+          for (int qq = 1; qq < 4; ++qq) mt = fmaxf(mt, red[(cg * 4 + qq) * 32 + lane]);
+          mnew_s[col0 + lane] = fmaxf(m_s[col0 + lane], mt);
+        }
+        tc::named_bar(1, nsm);
+        // factors 2^(m_old - m_new) for the running sums ...
+#pragma unroll
+        for (int c = 0; c < C::NC; ++c) {
+          const float mo = m_s[col0 + c], mn = mnew_s[col0 + c];
+          lpart[c] *= (mn == mo) ? 1.f : fast_exp2(mo - mn);
+        }
+        if (j > 0) {
+          // ... and for the O^T columns, once P.V of the previous tile is done
+          alive = alive && tc::mbar_wait(bar(kPvDone), (j - 1) & 1, abort_f, LIM);
+          if (alive) {
+            tc::tc_fence_after();
+#pragma unroll
+            for (int mh = 0; mh < C::MH; ++mh) {
+#pragma unroll
+              for (int c8 = 0; c8 < C::NC / 8; ++c8) {
+                const uint32_t ta = tbase + lane_off + C::OCOL + mh * C::SC + col0 + c8 * 8;
+                uint32_t r[8];
+                tc::tmem_ld8(ta, r);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float mo = m_s[col0 + c8 * 8 + e], mn = mnew_s[col0 + c8 * 8 + e];
+                  const float f = (mn == mo) ? 1.f : fast_exp2(mo - mn);
+                  r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                }
+                tc::tmem_st8(ta, r);
+              }
+            }
+            tc::tmem_wait_st();
+          }
+        }
+        tc::named_bar(1, nsm);  // every thread has read the old maxima
+        if (q == 0 && lane < C::NC) {
+          const float mn = mnew_s[col0 + lane];
+          m_s[col0 + lane] = mn;
+          base_s[col0 + lane] = mn == -kInf ? 0.f : mn;
+          thr_s[col0 + lane] = (mn + kTau) / alpha;
+        }
+        tc::named_bar(1, nsm);  // new maxima visible
+      }
+      // the single P buffer is free once P.V of the previous tile is done
+      if (j > 0) alive = alive && tc::mbar_wait(bar(kPvDone), (j - 1) & 1, abort_f, LIM);
+      // p = 2^(t - m): FP16 into P^T (MN-major, 128-byte swizzle); the row
+      // sums add the same rounded values
+      const int kt = 32 * q + lane;  // key within the tile
+#pragma unroll
+      for (int c8 = 0; c8 < C::NC / 8; ++c8) {
+        uint32_t hw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c8 * 8 + 2 * e;
+          const __half2 hh =
+              __floats2half2_rn(fast_exp2(fmaf(s[c], alpha, -base_s[col0 + c])),
+                                fast_exp2(fmaf(s[c + 1], alpha, -base_s[col0 + c + 1])));
+          const float2 fl = __half22float2(hh);
+          lpart[c] += fl.x;
+          lpart[c + 1] += fl.y;
+          hw[e] = *reinterpret_cast<const uint32_t *>(&hh);
+        }
+        const int r0 = col0 + c8 * 8;
+        *reinterpret_cast<uint4 *>(gP + sw128((uint32_t)(kt * 128 + (r0 >> 3) * 16))) =
+            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(kPReady));
+    }
+
+    // ---- epilogue: row sums and the unnormalised O^T of this partition
+#pragma unroll
+    for (int c = 0; c < C::NC; ++c) {
+      float sm = lpart[c];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      if (lane == 0) red[warp * 32 + c] = sm;
+    }
+    alive = alive && tc::mbar_wait(bar(kPvDone), (ntiles - 1) & 1, abort_f, LIM);
+    if (alive) {
+      tc::tc_fence_after();
+      const int64_t slot = ((int64_t)(b * p.Hkv + h) * p.P + part) * p.rows_pad + row0;
+#pragma unroll
+      for (int mh = 0; mh < C::MH; ++mh) {
+        const int d = 128 * mh + 32 * q + lane;
+#pragma unroll
+        for (int c8 = 0; c8 < C::NC / 8; ++c8) {
+          uint32_t r[8];
+          tc::tmem_ld8(tbase + lane_off + C::OCOL + mh * C::SC + col0 + c8 * 8, r);
+          tc::tmem_wait_ld();
+          if (d < D) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              // stored as sum p * dec(V) * 2^-8 (exact scaling): the
+              // combine kernel's convention
+              p.ws_o[(slot + col0 + c8 * 8 + e) * D + d] = __uint_as_float(r[e]) * 0.00390625f;
+            }
+          }
+        }
+      }
+    }
+    tc::tc_fence_before();
+  }
+
+  // ---- wind-down: drain copies and MMAs, free TMEM, publish (max, sum)
+  __syncthreads();
+  if ((warp == kWKProd || warp == kWVProd) && lane == 0) {
+    // every issued load must have landed before the CTA's memory is released
+    const int fullb = warp == kWVProd ? kVFull : kKFull;
+    const int nslot = warp == kWVProd ? C::NVR : C::NKR;
+    volatile int no_abort = 0;
+    for (int s = 0; s < nslot; ++s)
+      if (issued[s] > 0) tc::mbar_wait(bar(fullb + s), (issued[s] - 1) & 1, &no_abort, LIM);
+  }
+  if ((warp == kWQk || warp == kWPv) && lane == 0 && mma_issued) {
+    const uint32_t db = bar(warp == kWQk ? kDrainQk : kDrainPv);
+    tc::mma_commit(db);
+    volatile int no_abort = 0;
+    tc::mbar_wait(db, 0, &no_abort, LIM);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == kWQk) tc::tmem_dealloc(tbase, 512);
+  const bool aborted = *abort_f != 0, bad = *bad_f != 0;
+  if (tid == 0) {
+    if (aborted) atomicOr(p.status, VAE4_STATUS_TIMEOUT);
+    if (bad) atomicOr(p.status, VAE4_STATUS_BAD_BLOCK);
+  }
+  if (tid < N) {
+    const int r = tid, cg = r / C::NC, c = r - cg * C::NC;
+    float l = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) l += red[(cg * 4 + qq) * 32 + c];
+    const int64_t slot = ((int64_t)(b * p.Hkv + h) * p.P + part) * p.rows_pad + row0;
+    p.ws_ml[(slot + r) * 2 + 0] = m_s[r];
+    p.ws_ml[(slot + r) * 2 + 1] = (aborted || bad) ? -1.f : l;
+  }
+}
+
+}  // namespace vae4

@@ -86,8 +86,14 @@ typedef struct {
   int32_t max_seq_len;      /* launch capacity in tokens; 0 ->
                                block_table columns * page size */
   int32_t num_sms;          /* SMs the plan targets; 0 -> current device */
-  int32_t flags;            /* reserved, must be 0 */
+  int32_t flags;            /* 0, or VAE4_FLAG_WARP_MMA */
 } vae4_options;
+
+/* Option flag: run the split stage on the warp-level tensor-core path
+ * (mma.sync m16n8k16 with ldmatrix operands) instead of the default
+ * tcgen05 / TMEM / TMA kernel.  Same contract and precision; kept as the
+ * measured legacy baseline. */
+#define VAE4_FLAG_WARP_MMA 0x1
 
 /* Return codes. */
 enum vae4_error {
@@ -103,7 +109,7 @@ enum vae4_error {
   VAE4_ERR_CUDA = -9,        /* a CUDA runtime call failed */
   VAE4_ERR_PARTITION = -10,  /* partition_tokens not a positive multiple of 16,
                                 or more than 8192 partitions per sequence */
-  VAE4_ERR_OPTIONS = -11     /* nonzero reserved option flags */
+  VAE4_ERR_OPTIONS = -11     /* unknown option flags or a negative scale */
 };
 
 /* Bits of the device status word (sticky until verify_attn_e4m3_clear_status). */
@@ -221,15 +227,18 @@ int verify_attn_e4m3_read_status(const vae4_tensor *workspace,
 int verify_attn_e4m3_clear_status(const vae4_tensor *workspace, vae4_stream stream);
 
 /*
- * verify_attn_e4m3_decode_table -- test hook for the exact decoder: runs the
- * kernels' E4M3 -> FP16 decode routine on all 256 byte codes and writes the
- * raw FP16 bit patterns to dev_out (device, 256 x uint16).  The decoder maps
- * byte b to dec(b) * 2^scale_log2 exactly; *scale_log2 (host pointer)
- * receives that exponent (the kernels fold 2^-scale_log2 into their FP32
- * scales).  NaN codes 0x7F / 0xFF decode to a finite pattern and are outside
- * the contract.  ("exhaustive E4M3 bytes", PR #566, Test Result.)
+ * verify_attn_e4m3_decode_table -- test hook for the exact decoders: runs a
+ * split kernel's E4M3 -> FP16 decode routine on all 256 byte codes and
+ * writes the raw FP16 bit patterns to dev_out (device, 256 x uint16).
+ * flags selects the kernel as in vae4_options.flags: 0 = the tcgen05 path
+ * (hardware converter, dec(b) exactly), VAE4_FLAG_WARP_MMA = the mma.sync
+ * path (integer bit move, dec(b) * 2^-8 exactly).  *scale_log2 (host
+ * pointer) receives the exponent e with FP16 = dec(b) * 2^e; the kernels
+ * fold 2^-e into their FP32 scales.  The NaN codes 0x7F / 0xFF are outside
+ * the contract (NaN on the first decoder, a finite pattern on the second).
+ * ("exhaustive E4M3 bytes", PR #566, Test Result.)
  */
-int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2,
+int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2, int32_t flags,
                                   vae4_stream stream);
 
 /* Bytes of the library-owned scratch that verify_attn_e4m3_noalloc uses. */

@@ -30,14 +30,16 @@ def _gpu():
     vae4.load()
 
 
-def run_gpu(w, seq_len=None, q_len=None, partition_tokens=None, tensors=None, ws=None):
+def run_gpu(w, seq_len=None, q_len=None, partition_tokens=None, tensors=None, ws=None,
+            flags=0):
     q, kv, bt, seq, sc = tensors or W.to_device(w, seq_len=seq_len, q_len=q_len)
     s = w.spec
     T = s.partition_tokens if partition_tokens is None else partition_tokens
     out = torch.full_like(q, float("nan"))  # every element must be written
     if ws is None:
         ws = vae4.alloc_workspace(s.B, s.Hq, s.Hkv, s.Qmax, s.D, w.capacity, T)
-    vae4.verify(q, kv, bt, seq, sc, out, ws, partition_tokens=T, max_seq_len=w.capacity)
+    vae4.verify(q, kv, bt, seq, sc, out, ws, partition_tokens=T, max_seq_len=w.capacity,
+                flags=flags)
     torch.cuda.synchronize()
     return out.cpu().numpy(), ws
 
@@ -77,14 +79,15 @@ def check_full(w, **kw):
 
 
 # ------------------------------------------------------------------ decode
-def test_decode_table_is_exact():
-    bits, e = vae4.decode_table()
+@pytest.mark.parametrize("flags", [0, 1], ids=["tcgen05-path", "mma-sync-path"])
+def test_decode_table_is_exact(flags):
+    bits, e = vae4.decode_table(flags)
     torch.cuda.synchronize()
     h = bits.cpu().numpy().view(np.float16).astype(np.float64) * 2.0 ** (-e)
     t = oracle.e4m3_table()
     finite = [b for b in range(256) if b not in (0x7F, 0xFF)]
     assert np.array_equal(h[finite], t[finite])
-    assert np.isfinite(h).all()  # NaN codes decode to a finite pattern
+    assert e == (0 if flags == 0 else -8)
 
 
 # ----------------------------------------------------------- small, full
@@ -125,6 +128,27 @@ def test_parity_small(cfg):
         cfg.pop("name", None)
         w = W.custom("small", **cfg)
     check_full(w)
+
+
+@pytest.mark.parametrize("cfg", [SMALL[0], SMALL[1], SMALL[4], SMALL[11]],
+                         ids=["tiny", "41", "44", "51"])
+def test_parity_warp_mma_path(cfg):
+    """The legacy mma.sync split kernel (VAE4_FLAG_WARP_MMA) meets the same bar."""
+    cfg = dict(cfg)
+    w = W.generate(cfg["spec"]) if "spec" in cfg else W.custom(
+        "small", **{k: v for k, v in cfg.items() if k != "name"})
+    check_full(w, flags=vae4.FLAG_WARP_MMA)
+
+
+def test_paths_agree():
+    """Both split kernels on the same inputs: each within tolerance of the
+    oracle, and close to each other (different FP32 summation orders)."""
+    w = W.custom("both", B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[4000, 2222], q_lens=[8, 6],
+                 seed=56, partition_tokens=768)
+    a, _ = run_gpu(w)
+    b, _ = run_gpu(w, flags=vae4.FLAG_WARP_MMA)
+    d = np.abs(a.astype(np.float64) - b.astype(np.float64))
+    assert d.max() <= 2e-3
 
 
 def test_parity_auto_plan():
