@@ -128,19 +128,6 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def record_in_graph(event, stream):
-    """Record `event` as an event node of the graph being captured on
-    `stream` (an external record, so its timestamp is readable afterwards;
-    a plain record during capture only orders the capture)."""
-    import ctypes
-    lib = ctypes.CDLL("libcuda.so.1")
-    rc = lib.cuEventRecordWithFlags(ctypes.c_void_p(event.cuda_event),
-                                    ctypes.c_void_p(stream.cuda_stream),
-                                    ctypes.c_uint(1))  # CU_EVENT_RECORD_EXTERNAL
-    if rc != 0:
-        raise RuntimeError(f"cuEventRecordWithFlags failed: {rc}")
-
-
 def cpu_oracle_step(w, rows, threads=0):
     import oracle
     t0 = time.perf_counter()
@@ -227,49 +214,52 @@ def main():
     torch.cuda.synchronize()
     assert vae4.read_status(ws) == 0
 
-    # The timed steps are captured once into a CUDA graph (the pages time their
-    # kernels the same way) so host launch overhead stays out of the device
-    # timeline; CUDA events inside the graph bracket every split launch.
+    # Timed steps are captured into CUDA graphs (the pages time their kernels
+    # as graph replays too), so host launch overhead stays out of the device
+    # timeline.  Region 1: K whole steps (split + combine, the combine a
+    # programmatic dependent launch), events only around the replay -> value.
+    # Region 2: K back-to-back split launches -> the split kernel's mean
+    # launch time for the roofline.  Both rotate the KV pool copies.
     stream = torch.cuda.Stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):  # warm the launch path on the capture stream
         vae4.verify(q, kvs[0], bt, seq, sc, out, ws, **kw)
-        for a, b in ev:  # materialise the event handles before capture
-            a.record()
-            b.record()
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
+    g_step, g_split = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
         for k in range(args.steps):
-            a, b = ev[k]
-            record_in_graph(a, stream)
+            vae4.verify(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
+    with torch.cuda.graph(g_split, stream=stream):
+        for k in range(args.steps):
             vae4.verify_attn_e4m3_partials(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
-            record_in_graph(b, stream)
-            vae4.verify_attn_e4m3_combine(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
     torch.cuda.synchronize()
-    graph.replay()  # one untimed replay: graph upload and first-touch costs
+    with torch.cuda.stream(stream):  # untimed replays: upload and first touch
+        g_step.replay()
+        g_split.replay()
     torch.cuda.synchronize()
+
+    def timed(graph):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record()
+            graph.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return e0.elapsed_time(e1)
 
     uuid = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{uuid}" if uuid else None)
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        start.record()
-        graph.replay()
-        end.record()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    total_ms = timed(g_step)
+    split_total_ms = timed(g_split)
     clocks = sampler.stop()
-    total_ms = start.elapsed_time(end)
-    split_us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+    split_mean_us = split_total_ms * 1e3 / args.steps
     assert vae4.read_status(ws) == 0
     gpu_launches = 2 * args.steps
     stream = torch.cuda.current_stream()
@@ -307,7 +297,7 @@ def main():
 
     if rank == 0:
         peak, peak_kind = peaks()
-        split_mean = statistics.mean(split_us)
+        split_mean = split_mean_us
         achieved = kv_bytes / (split_mean * 1e-6) / 1e9
         traffic = kernel_traffic()
         rows = all_rows(w)
@@ -323,16 +313,15 @@ def main():
             "data": "synthetic",
             "config": {"workload": workload_desc(w), "seed": s.seed,
                        "partition_tokens": T_eff, "partitions": P,
-                       "timing": f"{args.steps} steps in one CUDA graph replay; split kernel "
-                                 "bracketed by events inside the graph",
+                       "timing": f"{args.steps} steps in one CUDA graph replay",
                        "l2": f"inputs rotate over {R} KV pool copies of {pool_bytes >> 20} MiB "
                              f"(> 3x the {l2 >> 20} MiB L2)"},
             "pct_of_hbm_peak": 100.0 * value / world / peak,
             "roofline": {"bound": "hbm", "kernel": "split (partials)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                         "traffic": traffic,
-                         "split_us_mean": split_mean, "split_us_median": statistics.median(split_us)},
+                         "traffic": traffic, "split_us_mean": split_mean,
+                         "timing": f"{args.steps} back-to-back split launches in one CUDA graph"},
             "cpu_baseline": {"value": kv_bytes / cpu_s / 1e9, "unit": "GB/s",
                              "cores": oracle.max_threads(), "kind": "oracle",
                              "sample": f"one full step: all {n_cpu} output rows, FP64",

@@ -21,28 +21,33 @@ namespace vae4 {
 namespace {
 
 constexpr int kCombineThreads = 256;
+constexpr int kLanes = 16;                          // float4 lanes: 64 d per CTA
+constexpr int kGroups = kCombineThreads / kLanes;   // partition groups
 
-// One CTA per output row (r, h, b).  Partition weights are computed once into
-// shared memory; the P.V partials are then summed by kCombineThreads/(D/4)
-// groups of threads, group k taking partitions k, k+ngrp, ... in ascending
-// order, and the group sums are added in group order: a fixed summation order
-// that does not depend on scheduling, so repeated runs agree bit for bit.
-template <int D>
+// One CTA per (output row, 64-wide slice of d).  Every CTA of a row computes
+// the row's partition weights into shared memory (a few hundred floats);
+// the P.V partials of its slice are then summed by kGroups groups of
+// threads, group k taking partitions k, k + kGroups, ... in ascending order,
+// and the group sums are added in group order: a fixed summation order that
+// does not depend on scheduling, so repeated runs agree bit for bit.  Many
+// short independent loads per thread keep the L2 busy instead of waiting on
+// one long dependent chain.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
   extern __shared__ __align__(16) float csm[];
-  constexpr int LANES = D / 4;                      // float4 lanes per row
-  constexpr int NGRP = kCombineThreads / LANES;     // partition groups
   __shared__ float red[kCombineThreads / 32];
-  __shared__ float4 accs[NGRP][LANES];
+  __shared__ float4 accs[kGroups][kLanes];
 
   // wait until the split kernel's partials are complete and visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
-  const int r = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int nd = p.D / 64;  // d slices per row
+  const int r = blockIdx.x / nd, dsl = blockIdx.x - r * nd;
+  const int h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = r / p.G, g = r - i * p.G;
+  const int d0 = dsl * 64;
   __half *out = static_cast<__half *>(p.out) + (int64_t)b * p.o_sb + (int64_t)i * p.o_si +
-                (int64_t)(h * p.G + g) * p.o_sh;
+                (int64_t)(h * p.G + g) * p.o_sh + d0;
 
   const int L = p.seq[(int64_t)b * p.seq_sb];
   const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
@@ -51,18 +56,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
   float *wm = csm;       // m_p, then the weight w_p
   float *wl = csm + p.P; // l_p
-  const int64_t pstride = (int64_t)p.rows_pad;
+  const int64_t pstride = (int64_t)p.rows_pad;  // rows per partition
   const float *ml = p.ws_ml + (int64_t)(b * p.Hkv + h) * p.P * pstride * 2 + r * 2;
   const float kNegInf = -__int_as_float(0x7f800000);
 
-  // ---- pass 1: load (m_p, l_p), maximum over partitions with l_p > 0
+  // ---- pass 1: (m_p, l_p), maximum over partitions with l_p > 0
   float mx = kNegInf;
   bool bad = false;
   for (int q = tid; q < nP; q += kCombineThreads) {
     const float2 v = *reinterpret_cast<const float2 *>(ml + q * pstride * 2);
     wm[q] = v.x;
     wl[q] = v.y;
-    if (v.y < 0.f) bad = true;  // a partition met an invalid page
+    if (v.y < 0.f) bad = true;  // a partition met an invalid page or timed out
     if (v.y > 0.f) mx = fmaxf(mx, v.x);
   }
 #pragma unroll
@@ -90,14 +95,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 #pragma unroll
   for (int k = 0; k < kCombineThreads / 32; ++k) Lam += red[k];
 
-  // ---- pass 3: sum of w_p * O_p per group, then over groups
-  const int l4 = tid % LANES, grp = tid / LANES;
-  const float *o = p.ws_o + (int64_t)(b * p.Hkv + h) * p.P * pstride * D + (int64_t)r * D + 4 * l4;
+  // ---- pass 3: sum of w_p * O_p over this slice, per group, then over groups
+  const int l4 = tid % kLanes, grp = tid / kLanes;
+  const float *o = p.ws_o + (int64_t)(b * p.Hkv + h) * p.P * pstride * p.D + (int64_t)r * p.D +
+                   d0 + 4 * l4;
+  const int64_t ostride = pstride * p.D;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int q = grp; q < nP; q += NGRP) {
+#pragma unroll 8
+  for (int q = grp; q < nP; q += kGroups) {
     const float w = wm[q];
-    const float4 v = *reinterpret_cast<const float4 *>(o + q * pstride * D);
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(o + q * ostride));
     acc.x += w * v.x;
     acc.y += w * v.y;
     acc.z += w * v.z;
@@ -108,7 +115,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   if (grp != 0) return;
   float4 s = accs[0][l4];
 #pragma unroll
-  for (int k = 1; k < NGRP; ++k) {
+  for (int k = 1; k < kGroups; ++k) {
     const float4 v = accs[k][l4];
     s.x += v.x;
     s.y += v.y;
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   }
   uint2 res = make_uint2(0u, 0u);
   if (!dead && !any_bad && Lam > 0.f) {
-    const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // V holds dec*2^-8
+    const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // partials hold dec(V) * 2^-8
     const __half2 lo = __floats2half2_rn(__fdiv_rn(s.x, Lam) * beta, __fdiv_rn(s.y, Lam) * beta);
     const __half2 hi = __floats2half2_rn(__fdiv_rn(s.z, Lam) * beta, __fdiv_rn(s.w, Lam) * beta);
     res.x = *reinterpret_cast<const uint32_t *>(&lo);
@@ -144,8 +151,9 @@ __global__ void decode_table_kernel(uint16_t *out, bool integer_path) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
+  if (p.D % 64 != 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.Qmax * p.G, p.Hkv, p.B);
+  cfg.gridDim = dim3(p.Qmax * p.G * (p.D / 64), p.Hkv, p.B);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float);
   cfg.stream = stream;
@@ -155,19 +163,12 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int smem = (int)cfg.dynamicSmemBytes;
-  switch (p.D) {
-    case 64:
-      cudaFuncSetAttribute(combine_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      return cudaLaunchKernelEx(&cfg, combine_kernel<64>, p);
-    case 128:
-      cudaFuncSetAttribute(combine_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      return cudaLaunchKernelEx(&cfg, combine_kernel<128>, p);
-    case 256:
-      cudaFuncSetAttribute(combine_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      return cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
-    default:
-      return cudaErrorInvalidValue;
+  if (smem > 48 * 1024) {  // beyond the default dynamic shared-memory limit
+    const cudaError_t e =
+        cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
   }
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 cudaError_t launch_decode_table(uint16_t *out, bool integer_path, cudaStream_t stream) {

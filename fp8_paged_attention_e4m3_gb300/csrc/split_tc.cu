@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -31,9 +32,17 @@ template <int D, int N>
 cudaError_t launch(const SplitParams &p, const TcArgs &a, const CUtensorMap &map,
                    cudaStream_t stream) {
   using C = TcCfg<D, N>;
-  cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<D, N>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is a per-device function attribute: set it once
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<D, N>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
   split_tc_kernel<D, N><<<dim3(p.P, p.Hkv * a.n_rg, p.B), C::NTHREADS, C::SMEM, stream>>>(p, a,
                                                                                           map);
   return cudaGetLastError();
@@ -72,12 +81,14 @@ cudaError_t launch_split_tc(const SplitParams &p, long long wait_limit, cudaStre
   a.wait_limit = wait_limit;
   a.n_rg = n_rg;
   if (a.rows_total > (int64_t)0x7fffff00) return cudaErrorInvalidValue;
+  // the pool as a 3-D tensor: (byte within an IB-wide block, row of D bytes,
+  // block of the row); a box of {IB, 16, D/IB} is one 16-key page slice
   CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)a.rows_total};
-  const cuuint64_t strides[1] = {(cuuint64_t)D};
-  const cuuint32_t box[2] = {(cuuint32_t)IB, 16u};
-  const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+  const cuuint64_t dims[3] = {(cuuint64_t)IB, (cuuint64_t)a.rows_total, (cuuint64_t)(D / IB)};
+  const cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)IB};
+  const cuuint32_t box[3] = {(cuuint32_t)IB, 16u, (cuuint32_t)(D / IB)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
                             const_cast<uint8_t *>(p.kv), dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE,
                             IB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,

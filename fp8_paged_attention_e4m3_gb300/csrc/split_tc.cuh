@@ -5,12 +5,13 @@
 // context is walked in 128-key tiles made of two 64-key half-tiles.
 // Warp roles (20 warps):
 //
-//   K / V producer  : one thread each walks the block table and issues TMA
-//                     tensor loads (128-byte swizzle) of the E4M3 K (resp. V)
-//                     page slices of a half-tile into its own ring (K: 2
-//                     slots, V: 2 or 3).  Keys past the partition and pages
-//                     with invalid ids are loaded from outside the tensor,
-//                     which fills zeros.
+//   K / V producer  : one warp each walks the block table (32 entries per
+//                     load, prefetched one batch ahead into registers) and
+//                     issues TMA tensor loads (128-byte swizzle), one 16 x D
+//                     byte page slice per load, of the E4M3 K (resp. V) of
+//                     a half-tile into its own ring (K: 2 slots, V: 2 or 3).
+//                     Keys past the partition and pages with invalid ids are
+//                     loaded from outside the tensor, which fills zeros.
 //   K decoders (4)  : thread = key; exact E4M3 -> FP16 with the hardware
 //                     converter, straight into tensor memory: the A operand
 //                     of S^T = K . Q^T (lane = key, column = pair of d).
@@ -234,35 +235,45 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
 
   if (warp == kWKProd || warp == kWVProd) {
     // =============================== producers (K ring, V ring)
-    if (lane == 0) {
-      const bool isv = warp == kWVProd;
-      const int nslot = isv ? C::NVR : C::NKR;
-      const int fullb = isv ? kVFull : kKFull, emptyb = isv ? kVEmpty : kKEmpty;
-      const uint32_t ring = isv ? sVR : sKR;
-      tc::prefetch_tensormap(&tmap);
-      const int page_shift = __ffs(p.page) - 1;
-      for (int t = 0; t < nhalf; ++t) {
-        const int st = t % nslot, u = t / nslot;
-        if (t >= nslot && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
-        tc::mbar_arrive_expect_tx(bar(fullb + st), C::RSLOT);
-        issued[st] = u + 1;
+    const bool isv = warp == kWVProd;
+    const int nslot = isv ? C::NVR : C::NKR;
+    const int fullb = isv ? kVFull : kKFull, emptyb = isv ? kVEmpty : kKEmpty;
+    const uint32_t ring = isv ? sVR : sKR;
+    const int page_shift = __ffs(p.page) - 1;
+    const int lp_end = (k1 + p.page - 1) >> page_shift;  // pages of this partition end here
+    const int32_t *btb = p.bt + (int64_t)b * p.bt_sb;
+    // block-table entries for logical pages [lp_base, lp_base + 64): lane l
+    // holds lp_base + l (cur) and lp_base + 32 + l (nxt)
+    int lp_base = k0 >> page_shift;
+    auto fetch = [&](int lp) -> int { return lp < lp_end ? __ldg(btb + lp) : -1; };
+    int cur = fetch(lp_base + lane), nxt = fetch(lp_base + 32 + lane);
+    if (lane == 0) tc::prefetch_tensormap(&tmap);
+    for (int t = 0; t < nhalf; ++t) {
+      const int st = t % nslot, u = t / nslot;
+      if (t >= nslot && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
+      if (lane == 0) tc::mbar_arrive_expect_tx(bar(fullb + st), C::RSLOT);
+      issued[st] = u + 1;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int key0 = k0 + 64 * t + 16 * g;
+      for (int g = 0; g < 4; ++g) {
+        const int key0 = k0 + 64 * t + 16 * g;
+        const int lp = key0 >> page_shift;
+        while (lp >= lp_base + 32) {  // advance the register window (warp-uniform)
+          cur = nxt;
+          lp_base += 32;
+          nxt = fetch(lp_base + 32 + lane);
+        }
+        const int phys = __shfl_sync(0xffffffffu, cur, lp - lp_base);
+        if (lane == 0) {
           int row = (int)a.rows_total;  // outside the tensor: zero fill
           if (key0 < k1) {
-            const int lp = key0 >> page_shift;
-            const int phys = p.bt[(int64_t)b * p.bt_sb + lp];
             if (phys >= 0 && phys < p.n_pages)
               row = (int)(((int64_t)phys * 2 * p.Hkv + (isv ? p.Hkv : 0) + h) * p.page +
                           (key0 - (lp << page_shift)));
             else
               *bad_f = 1;
           }
-#pragma unroll
-          for (int dh = 0; dh < C::NDH; ++dh)
-            tc::tma_load_2d(ring + st * C::RSLOT + dh * (64 * C::IB) + g * (16 * C::IB), &tmap,
-                            dh * C::IB, row, bar(fullb + st));
+          // one box: 16 keys x D bytes, as NDH blocks of 16 x IB (swizzled)
+          tc::tma_load_3d(ring + st * C::RSLOT + g * (16 * D), &tmap, 0, row, 0, bar(fullb + st));
         }
       }
     }
@@ -342,9 +353,10 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
           for (int q4 = 0; q4 < 4; ++q4) {
             const int c = grp * 4 + q4;  // 16-byte chunk of the key row
             const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
-            const uint32_t off = (uint32_t)(kk * C::IB + cc * 16);
+            const uint32_t off = (uint32_t)((kk & 15) * C::IB + cc * 16);
             const uint4 w = *reinterpret_cast<const uint4 *>(
-                rawK + dh * (64 * C::IB) + (off ^ (((off >> 7) & C::SMASK) << 4)));
+                rawK + (kk >> 4) * (16 * D) + dh * (16 * C::IB) +
+                (off ^ (((off >> 7) & C::SMASK) << 4)));
             e4m3x4_to_f16x4_hw(w.x, r[q4 * 8 + 0], r[q4 * 8 + 1]);
             e4m3x4_to_f16x4_hw(w.y, r[q4 * 8 + 2], r[q4 * 8 + 3]);
             e4m3x4_to_f16x4_hw(w.z, r[q4 * 8 + 4], r[q4 * 8 + 5]);
@@ -373,9 +385,10 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
 #pragma unroll 4
         for (int c = 0; c < D / 16; ++c) {
           const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
-          const uint32_t off = (uint32_t)(kk * C::IB + cc * 16);
+          const uint32_t off = (uint32_t)((kk & 15) * C::IB + cc * 16);
           const uint4 w = *reinterpret_cast<const uint4 *>(
-              rawV + dh * (64 * C::IB) + (off ^ (((off >> 7) & C::SMASK) << 4)));
+              rawV + (kk >> 4) * (16 * D) + dh * (16 * C::IB) +
+              (off ^ (((off >> 7) & C::SMASK) << 4)));
           uint4 h0, h1;
           e4m3x16_to_f16x16_hw(w, h0, h1);
           const int dblk = c >> 2, c2 = 2 * (c & 3);
