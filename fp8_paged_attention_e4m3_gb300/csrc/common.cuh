@@ -108,6 +108,18 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
       : "r"(addr));
 }
+// Two transposed 16 x 16 byte matrices (threads 0-15 give the 16 row
+// addresses of the first, 16-31 of the second): thread i receives, of the
+// first matrix, rows 4(i%4) .. 4(i%4)+3 of column i/4 in r[0] (row order
+// = byte order) and of column i/4 + 8 in r[1]; r[2], r[3] likewise for
+// the second matrix.
+__device__ __forceinline__ void ldsm_b8_trans_x2(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(addr)
+      : "memory");
+}
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4],
                                          uint32_t b0, uint32_t b1) {
   asm volatile(

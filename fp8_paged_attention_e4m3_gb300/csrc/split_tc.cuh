@@ -6,21 +6,28 @@
 // Warp roles (20 warps):
 //
 //   K / V producer  : one warp each walks the block table (32 entries per
-//                     load, prefetched one batch ahead into registers) and
-//                     issues TMA tensor loads (128-byte swizzle), one 16 x D
-//                     byte page slice per load, of the E4M3 K (resp. V) of
-//                     a half-tile into its own ring (K: 2 slots, V: 2 or 3).
-//                     Keys past the partition and pages with invalid ids are
+//                     load, prefetched one batch ahead into registers, the
+//                     first batch before the CTA's set-up) and issues TMA
+//                     tensor loads (128-byte swizzle), one 16 x D byte page
+//                     slice per load, of the E4M3 K (resp. V) of a half-tile
+//                     into its own ring of raw slots (5-8 slots each: the
+//                     shared memory holds only raw bytes, Q and P).  Keys
+//                     past the partition and pages with invalid ids are
 //                     loaded from outside the tensor, which fills zeros.
 //   K decoders (4)  : thread = key; exact E4M3 -> FP16 with the hardware
 //                     converter, straight into tensor memory: the A operand
 //                     of S^T = K . Q^T (lane = key, column = pair of d).
-//   V decoders (4)  : thread = key; same decode into a 3-slot ring of FP16
-//                     V^T half-tiles in shared memory (MN-major, 128-byte
-//                     swizzle), so V is decoded as soon as it lands.
+//   V decoders (4)  : warp = 32 d of every 128-d block, all 64 keys of a
+//                     half-tile: a transposing 8-bit ldmatrix of 16 keys x
+//                     16 d gives each thread four consecutive keys of one d,
+//                     which after the same exact conversion is a 16x256b
+//                     tensor-memory store fragment: V^T lands in TMEM as the
+//                     A operand of O^T = V^T . P^T (lane = d, column = pair
+//                     of keys), in a ring of 2-4 half-tile slots.
 //   score MMA warp  : issues tcgen05.mma.kind::f16  S^T[128 x N] = K . Q^T
 //   value MMA warp  : issues tcgen05.mma.kind::f16  O^T[d x N] += V^T . P^T
-//                     (FP32 accumulators in TMEM; commits to mbarriers).
+//                     (both with A in TMEM and B in shared memory; FP32
+//                     accumulators in TMEM; commits to mbarriers).
 //   softmax (8)     : thread = key, half of the N rows each; loads S^T from
 //                     TMEM, applies the causal / partition mask at the
 //                     edges, keeps the FP32 running max per row (raised
@@ -69,22 +76,24 @@ struct TcCfg {
   static constexpr int DB = D / 64 < 2 ? 2 : D / 64;  // 64-d blocks of V^T (D=64 padded)
   static constexpr int MH = DB / 2;             // 128-row M halves of V^T.P^T
   static constexpr int SC = (N + 31) / 32 * 32; // TMEM columns per accumulator
+  // TMEM columns: K (128 keys x D/2), two S^T buffers, O^T, then the V^T
+  // half-tile ring (lane = d of a 128-d block, 32 columns per block)
   static constexpr int KCOL = 0, SCOL = 128, OCOL = 128 + 2 * SC;
-  static constexpr int NKR = 2;                 // K raw slots (>= 2)
+  static constexpr int VCOL = OCOL + MH * SC;
+  static constexpr int VTC = MH * 32;           // columns per V^T half-tile
+  static constexpr int NVF = (512 - VCOL) / VTC < 4 ? (512 - VCOL) / VTC : 4;
   static constexpr int QB = (D / 64) * N * 128; // Q, K-major SW128
-  static constexpr int VSLOT = DB * 64 * 128;   // one FP16 V^T half-tile
   static constexpr int PB = 128 * 128;          // P^T, MN-major SW128 (N <= 64)
   static constexpr int RSLOT = 64 * D;          // one raw K or V half-tile
-  static constexpr int SMALL = 2688;
+  static constexpr int SMALL = 2880;
   static constexpr int LIMIT = 232448 - 1024;   // opt-in maximum minus alignment slack
-  // FP16 V^T slots and V raw slots (NVR >= NVF keeps the decoders' slot
-  // waits unambiguous): 3 and 3 when they fit, else 2 and 2
-  static constexpr bool FIT3 = QB + 3 * VSLOT + PB + (NKR + 3) * RSLOT + SMALL <= LIMIT;
-  static constexpr int NVF = FIT3 ? 3 : 2;
-  static constexpr int NVR = FIT3 ? 3 : 2;
+  // raw slots: whatever shared memory is left, split between the rings
+  // (NVR >= NVF keeps the V decoders' slot waits unambiguous)
+  static constexpr int NRAW = (LIMIT - QB - PB - SMALL) / RSLOT;
+  static constexpr int NKR = NRAW / 2 < 8 ? NRAW / 2 : 8;
+  static constexpr int NVR = NRAW - NKR < 8 ? NRAW - NKR : 8;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_V = OFF_Q + QB;
-  static constexpr int OFF_P = OFF_V + NVF * VSLOT;
+  static constexpr int OFF_P = OFF_Q + QB;
   static constexpr int OFF_KR = OFF_P + PB;
   static constexpr int OFF_VR = OFF_KR + NKR * RSLOT;
   static constexpr int OFF_SMALL = OFF_VR + NVR * RSLOT;
@@ -97,10 +106,10 @@ struct TcCfg {
                        B_SFULL = B_VFREE + NVF, B_SFREE = B_SFULL + 2, B_PREADY = B_SFREE + 2,
                        B_PVDONE = B_PREADY + 1, B_DRAINQK = B_PVDONE + 1,
                        B_DRAINPV = B_DRAINQK + 1, NBARS = B_DRAINPV + 1;
-  static_assert(NBARS * 8 <= 320, "barriers fit below the small-region scalars");
-  static_assert(NKR <= 4 && NVR <= 4, "producer bookkeeping");
-  static_assert(NKR >= 2 && NVR >= NVF, "slot reuse order (see the decoders)");
-  static_assert(OCOL + MH * SC <= 512, "TMEM budget");
+  static_assert(NBARS * 8 <= 512, "barriers fit below the small-region scalars");
+  static_assert(NKR <= 8 && NVR <= 8, "producer bookkeeping");
+  static_assert(NKR >= 2 && NVF >= 2 && NVR >= NVF, "slot reuse order (see the decoders)");
+  static_assert(VCOL + NVF * VTC <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NC % 8 == 0, "softmax column groups of 8");
 };
@@ -112,10 +121,10 @@ enum : int {
   kWVDec = 12,     // 12..15
   kWKProd = 16, kWVProd = 17, kWQk = 18, kWPv = 19
 };
-// offsets in the small region (the mbarriers occupy its first 320 bytes)
-constexpr int kSmTslot = 320, kSmAbort = 324, kSmBad = 328, kSmVotes = 352, kSmM = 384,
-              kSmPos = 640, kSmMNew = 896, kSmBase = 1152, kSmThr = 1408,
-              kSmRed = 1664;  // red: 8 warps x 32 floats
+// offsets in the small region (the mbarriers occupy its first 512 bytes)
+constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmVotes = 544, kSmM = 576,
+              kSmPos = 832, kSmMNew = 1088, kSmBase = 1344, kSmThr = 1600,
+              kSmRed = 1856;  // red: 8 warps x 32 floats, ends at 2880
 
 __device__ __forceinline__ uint32_t sw128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
 
@@ -136,10 +145,10 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
   uint8_t *gbase = smem_raw + (sbase - raw_addr);
-  const uint32_t sQ = sbase + C::OFF_Q, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P,
-                 sKR = sbase + C::OFF_KR, sVR = sbase + C::OFF_VR, sSm = sbase + C::OFF_SMALL;
-  uint8_t *gQ = gbase + C::OFF_Q, *gV = gbase + C::OFF_V, *gP = gbase + C::OFF_P,
-          *gKR = gbase + C::OFF_KR, *gVR = gbase + C::OFF_VR, *gSm = gbase + C::OFF_SMALL;
+  const uint32_t sQ = sbase + C::OFF_Q, sP = sbase + C::OFF_P, sKR = sbase + C::OFF_KR,
+                 sVR = sbase + C::OFF_VR, sSm = sbase + C::OFF_SMALL;
+  uint8_t *gQ = gbase + C::OFF_Q, *gP = gbase + C::OFF_P, *gKR = gbase + C::OFF_KR,
+          *gSm = gbase + C::OFF_SMALL;
   auto bar = [&](int i) -> uint32_t { return sSm + 8u * (uint32_t)i; };
   volatile int *abort_f = reinterpret_cast<volatile int *>(gSm + kSmAbort);
   volatile int *bad_f = reinterpret_cast<volatile int *>(gSm + kSmBad);
@@ -155,6 +164,21 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   const int part = blockIdx.x, b = blockIdx.z;
   const int h = blockIdx.y / a.n_rg, rg = blockIdx.y - h * a.n_rg;
   const int row0 = rg * N;  // first row of this CTA's row group
+  const bool producer = warp == kWKProd || warp == kWVProd;
+
+  // producers: first block-table window, requested before anything else so
+  // its latency overlaps the set-up.  Lane l holds logical page lp_base + l
+  // (cur) and lp_base + 32 + l (nxt); entries past the row are -1, entries
+  // past the sequence are loaded but never used.
+  const int page_shift = __ffs(p.page) - 1;
+  const int32_t *btb = p.bt + (int64_t)b * p.bt_sb;
+  auto fetch = [&](int lp) -> int { return lp < p.max_pages ? __ldg(btb + lp) : -1; };
+  int lp_base = (part * p.T) >> page_shift;
+  int cur = -1, nxt = -1;
+  if (producer) {
+    cur = fetch(lp_base + lane);
+    nxt = fetch(lp_base + 32 + lane);
+  }
 
   // ---- sequence, partition
   const int L = p.seq[(int64_t)b * p.seq_sb];
@@ -173,16 +197,18 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   const int ntiles = (k1 - k0 + 127) >> 7;
   const int nhalf = 2 * ntiles;  // half-tiles, the last may be all padding
 
-  // ---- set-up: barriers, queries, per-row state, TMEM
+  // ---- set-up: barriers and TMEM first (the producers start right after),
+  // then queries and per-row state (everyone else)
   if (tid == 0) {
-    // arrival counts: TMA (expect_tx) and MMA commits arrive once; a K or V
-    // half-tile is consumed by 2 decoder warps; K for a tile comes from 4.
+    // arrival counts: TMA (expect_tx) and MMA commits arrive once; a K
+    // half-tile is consumed by 2 decoder warps, a V half-tile by 4; K for a
+    // tile comes from 4.
     for (int i = 0; i < C::NBARS; ++i) {
       uint32_t cnt = 1;
-      if ((i >= kKEmpty && i < kKEmpty + C::NKR) || (i >= kVEmpty && i < kVEmpty + C::NVR) ||
-          (i >= kVReady && i < kVReady + C::NVF))
+      if (i >= kKEmpty && i < kKEmpty + C::NKR)
         cnt = 64;
-      else if (i == kKReady)
+      else if (i == kKReady || (i >= kVEmpty && i < kVEmpty + C::NVR) ||
+               (i >= kVReady && i < kVReady + C::NVF))
         cnt = 128;
       else if ((i >= kSFree && i < kSFree + 2) || i == kPReady)
         cnt = 32 * C::NSW;
@@ -191,10 +217,22 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     *abort_f = 0;
     *bad_f = 0;
   }
-  {
+  if (warp == kWQk) {
+    tc::tmem_alloc(sSm + kSmTslot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::mbar_fence_init();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(gSm + kSmTslot);
+  const long long LIM = a.wait_limit;
+  constexpr int kSetup = C::NTHREADS - 64;  // every thread but the producers
+  if (!producer) {
+    const int st_id = tid < 32 * kWKProd ? tid : tid - 64;
     const __half *qb = static_cast<const __half *>(p.q) + (int64_t)b * p.q_sb;
     constexpr int QCH = D / 8;  // 16-byte chunks per query row
-    for (int c = tid; c < N * QCH; c += C::NTHREADS) {
+    for (int c = st_id; c < N * QCH; c += kSetup) {
       const int r = c / QCH, cc = c - r * QCH;
       const int rr = row0 + r, i = rr / p.G, g = rr - i * p.G;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -204,49 +242,26 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
       const int katom = cc >> 3, c8 = cc & 7;
       *reinterpret_cast<uint4 *>(gQ + katom * (N * 128) + sw128(r * 128 + c8 * 16)) = v;
     }
-    for (int r = tid; r < N; r += C::NTHREADS) {
+    for (int r = st_id; r < N; r += kSetup) {
       const int rr = row0 + r, i = rr / p.G;
       pos_s[r] = (rr < p.rows && i < ql) ? L - ql + i : -1;
       m_s[r] = -kInf;
       base_s[r] = 0.f;
       thr_s[r] = -kInf;
     }
-    if (D == 64) {  // the padding 64-d block of every V^T slot reads as zeros
-      for (int c = tid; c < C::NVF * 512; c += C::NTHREADS) {
-        const int s = c >> 9, rem = c & 511;
-        *reinterpret_cast<uint4 *>(gV + s * C::VSLOT + 8192 + rem * 16) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
+    tc::fence_proxy_async_smem();  // Q is read by the tensor core
+    tc::named_bar(2, kSetup);
   }
-  if (warp == kWQk) {
-    tc::tmem_alloc(sSm + kSmTslot, 512);
-    tc::tmem_relinquish();
-  }
-  tc::fence_proxy_async_smem();
-  tc::mbar_fence_init();
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(gSm + kSmTslot);
-  const long long LIM = a.wait_limit;
 
-  int issued[4] = {0, 0, 0, 0};  // producers: uses issued per ring slot
+  int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // producers: uses issued per ring slot
   bool mma_issued = false;    // this thread issued tcgen05.mma
 
-  if (warp == kWKProd || warp == kWVProd) {
+  if (producer) {
     // =============================== producers (K ring, V ring)
     const bool isv = warp == kWVProd;
     const int nslot = isv ? C::NVR : C::NKR;
     const int fullb = isv ? kVFull : kKFull, emptyb = isv ? kVEmpty : kKEmpty;
     const uint32_t ring = isv ? sVR : sKR;
-    const int page_shift = __ffs(p.page) - 1;
-    const int lp_end = (k1 + p.page - 1) >> page_shift;  // pages of this partition end here
-    const int32_t *btb = p.bt + (int64_t)b * p.bt_sb;
-    // block-table entries for logical pages [lp_base, lp_base + 64): lane l
-    // holds lp_base + l (cur) and lp_base + 32 + l (nxt)
-    int lp_base = k0 >> page_shift;
-    auto fetch = [&](int lp) -> int { return lp < lp_end ? __ldg(btb + lp) : -1; };
-    int cur = fetch(lp_base + lane), nxt = fetch(lp_base + 32 + lane);
     if (lane == 0) tc::prefetch_tensormap(&tmap);
     for (int t = 0; t < nhalf; ++t) {
       const int st = t % nslot, u = t / nslot;
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   } else if (warp == kWPv) {
     // =============================== value MMA issuer: O^T += V^T . P^T
     if (lane == 0) {
-      constexpr uint32_t id_pv = tc::idesc_f16(128, N, 1, 1);
+      constexpr uint32_t id_pv = tc::idesc_f16(128, N, 0, 1);
       bool ok = true;
       for (int j = 0; ok && j < ntiles; ++j) {
         if (!(ok = tc::mbar_wait(bar(kPReady), j & 1, abort_f, LIM))) break;
@@ -313,10 +328,10 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
               const int ks = kh * 4 + k4;
-              const uint32_t av = sV + vs * C::VSLOT + (2 * mh) * 8192 + k4 * 2048;
+              const uint32_t av = tbase + C::VCOL + vs * C::VTC + mh * 32 + k4 * 8;
               const uint32_t bp = sP + ks * 2048;
-              tc::mma_ss(tbase + C::OCOL + mh * C::SC, tc::smem_desc(av, 8192, 1024),
-                         tc::smem_desc(bp, 16384, 1024), id_pv, (j > 0 || ks > 0) ? 1u : 0u);
+              tc::mma_ts(tbase + C::OCOL + mh * C::SC, av, tc::smem_desc(bp, 16384, 1024), id_pv,
+                         (j > 0 || ks > 0) ? 1u : 0u);
             }
           }
           tc::mma_commit(bar(kVFree + vs));
@@ -326,80 +341,100 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
         tc::mma_commit(bar(kPvDone));
       }
     }
-  } else if (warp >= kWKDec) {
-    // =============================== decoders (thread = key)
-    const bool isv = warp >= kWVDec;
+  } else if (warp >= kWKDec && warp < kWVDec) {
+    // =============================== K decoders (thread = key)
     const int dq = warp & 3;              // TMEM lane quadrant = keys 32*dq.. of a tile
     const int kh = dq >> 1;               // half-tile of the 128-key tile
     const int kk = 32 * (dq & 1) + lane;  // key within the half-tile
     const uint32_t lane_off = (uint32_t)(32 * dq) << 16;
     for (int j = 0; j < ntiles; ++j) {
       const int t = 2 * j + kh;
-      if (!isv) {
-        // K -> TMEM: column c holds d = 2c (low half), 2c+1 (high half).
-        // Wait for the previous tile's score MMA first: it proves every
-        // earlier K half-tile (in particular this slot's previous use, t -
-        // NKR <= t - 2) has landed and been read, so the parity wait on the
-        // slot below cannot match an older phase when pairs share slots.
-        const int st = t % C::NKR;
-        if (j > 0 && !tc::mbar_wait(bar(kKFree), (j - 1) & 1, abort_f, LIM)) break;
-        if (!tc::mbar_wait(bar(kKFull + st), (t / C::NKR) & 1, abort_f, LIM)) break;
-        tc::tc_fence_after();
-        const uint8_t *rawK = gKR + st * C::RSLOT;
+      // K -> TMEM: column c holds d = 2c (low half), 2c+1 (high half).
+      // Wait for the previous tile's score MMA first: it proves every
+      // earlier K half-tile (in particular this slot's previous use, t -
+      // NKR <= t - 2) has landed and been read, so the parity wait on the
+      // slot below cannot match an older phase when pairs share slots.
+      const int st = t % C::NKR;
+      if (j > 0 && !tc::mbar_wait(bar(kKFree), (j - 1) & 1, abort_f, LIM)) break;
+      if (!tc::mbar_wait(bar(kKFull + st), (t / C::NKR) & 1, abort_f, LIM)) break;
+      tc::tc_fence_after();
+      const uint8_t *rawK = gKR + st * C::RSLOT;
 #pragma unroll
-        for (int grp = 0; grp < D / 64; ++grp) {
-          uint32_t r[32];
+      for (int grp = 0; grp < D / 64; ++grp) {
+        uint32_t r[32];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int c = grp * 4 + q4;  // 16-byte chunk of the key row
-            const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
-            const uint32_t off = (uint32_t)((kk & 15) * C::IB + cc * 16);
-            const uint4 w = *reinterpret_cast<const uint4 *>(
-                rawK + (kk >> 4) * (16 * D) + dh * (16 * C::IB) +
-                (off ^ (((off >> 7) & C::SMASK) << 4)));
-            e4m3x4_to_f16x4_hw(w.x, r[q4 * 8 + 0], r[q4 * 8 + 1]);
-            e4m3x4_to_f16x4_hw(w.y, r[q4 * 8 + 2], r[q4 * 8 + 3]);
-            e4m3x4_to_f16x4_hw(w.z, r[q4 * 8 + 4], r[q4 * 8 + 5]);
-            e4m3x4_to_f16x4_hw(w.w, r[q4 * 8 + 6], r[q4 * 8 + 7]);
-          }
-          const uint32_t (&r0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[0]);
-          const uint32_t (&r1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[16]);
-          tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32, r0);
-          tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32 + 16, r1);
-        }
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        tc::mbar_arrive(bar(kKReady));
-        tc::mbar_arrive(bar(kKEmpty + st));
-      } else {
-        // V -> FP16 V^T slot (MN-major, 128-byte swizzle).  Wait for the
-        // value MMA that last read the FP16 slot first: it proves half-tiles
-        // up to t - NVF >= t - NVR were decoded, i.e. this raw slot's
-        // previous use is complete, so the parity wait below is unambiguous.
-        const int st = t % C::NVR, vs = t % C::NVF;
-        if (t >= C::NVF && !tc::mbar_wait(bar(kVFree + vs), ((t / C::NVF) - 1) & 1, abort_f, LIM))
-          break;
-        if (!tc::mbar_wait(bar(kVFull + st), (t / C::NVR) & 1, abort_f, LIM)) break;
-        const uint8_t *rawV = gVR + st * C::RSLOT;
-        uint8_t *vdst = gV + vs * C::VSLOT;
-#pragma unroll 4
-        for (int c = 0; c < D / 16; ++c) {
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int c = grp * 4 + q4;  // 16-byte chunk of the key row
           const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
           const uint32_t off = (uint32_t)((kk & 15) * C::IB + cc * 16);
           const uint4 w = *reinterpret_cast<const uint4 *>(
-              rawV + (kk >> 4) * (16 * D) + dh * (16 * C::IB) +
+              rawK + (kk >> 4) * (16 * D) + dh * (16 * C::IB) +
               (off ^ (((off >> 7) & C::SMASK) << 4)));
-          uint4 h0, h1;
-          e4m3x16_to_f16x16_hw(w, h0, h1);
-          const int dblk = c >> 2, c2 = 2 * (c & 3);
-          uint8_t *blk = vdst + dblk * 8192;
-          *reinterpret_cast<uint4 *>(blk + sw128((uint32_t)(kk * 128 + c2 * 16))) = h0;
-          *reinterpret_cast<uint4 *>(blk + sw128((uint32_t)(kk * 128 + (c2 + 1) * 16))) = h1;
+          e4m3x4_to_f16x4_hw(w.x, r[q4 * 8 + 0], r[q4 * 8 + 1]);
+          e4m3x4_to_f16x4_hw(w.y, r[q4 * 8 + 2], r[q4 * 8 + 3]);
+          e4m3x4_to_f16x4_hw(w.z, r[q4 * 8 + 4], r[q4 * 8 + 5]);
+          e4m3x4_to_f16x4_hw(w.w, r[q4 * 8 + 6], r[q4 * 8 + 7]);
         }
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(bar(kVReady + vs));
-        tc::mbar_arrive(bar(kVEmpty + st));
+        const uint32_t (&r0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[0]);
+        const uint32_t (&r1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[16]);
+        tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32, r0);
+        tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32 + 16, r1);
       }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(kKReady));
+      tc::mbar_arrive(bar(kKEmpty + st));
+    }
+  } else if (warp >= kWVDec) {
+    // =============================== V decoders (warp = 32 d per 128-d block)
+    const int dq = warp & 3;  // TMEM lane quadrant = d 32*dq.. of each 128-d block
+    // ldmatrix rows: threads 0-15 give keys 0-15 of a page, 16-31 the same
+    // rows of the next page (two 16 x 16 byte matrices per load)
+    const int pr = lane & 15, pg = lane >> 4;
+    for (int t = 0; t < nhalf; ++t) {
+      // V -> V^T in TMEM (lane = d, column c = keys 2c, 2c+1).  Wait for
+      // the value MMA that last read the V^T slot first: it proves
+      // half-tiles up to t - NVF >= t - NVR were decoded, i.e. this raw
+      // slot's previous use is complete, so the parity wait below is
+      // unambiguous.
+      const int st = t % C::NVR, vs = t % C::NVF;
+      if (t >= C::NVF && !tc::mbar_wait(bar(kVFree + vs), ((t / C::NVF) - 1) & 1, abort_f, LIM))
+        break;
+      if (!tc::mbar_wait(bar(kVFull + st), (t / C::NVR) & 1, abort_f, LIM)) break;
+      tc::tc_fence_after();
+      const uint32_t rawV = sVR + st * C::RSLOT;
+#pragma unroll
+      for (int mh = 0; mh < C::MH; ++mh) {
+#pragma unroll
+        for (int dc = 0; dc < 2; ++dc) {
+          const int dch = 128 * mh + 32 * dq + 16 * dc;  // first d of the 16-d chunk
+          if (dch < D) {
+            const int dh = dch / C::IB, cc = (dch % C::IB) >> 4;
+            const uint32_t off = (uint32_t)(pr * C::IB + cc * 16);
+            const uint32_t src = rawV + dh * (16 * C::IB) + (off ^ (((off >> 7) & C::SMASK) << 4));
+#pragma unroll
+            for (int kp = 0; kp < 2; ++kp) {  // keys 32 kp .. 32 kp + 31
+              uint32_t m4[4];
+              ldsm_b8_trans_x2(m4, src + (2 * kp + pg) * (16 * D));
+              // m4[0]: keys 4(l%4) + 0..3 of d = l/4, m4[1]: of d + 8;
+              // m4[2], m4[3]: the same for the keys 16 later
+              uint32_t v[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[2 * e] = cvt_e4m3x2(m4[e]);
+                v[2 * e + 1] = cvt_e4m3x2(m4[e] >> 16);
+              }
+              tc::tmem_st_16x256b_x2(tbase + ((uint32_t)(32 * dq + 16 * dc) << 16) + C::VCOL +
+                                         vs * C::VTC + mh * 32 + kp * 16,
+                                     v);
+            }
+          }
+        }
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(kVReady + vs));
+      tc::mbar_arrive(bar(kVEmpty + st));
     }
   } else {
     // =============================== softmax (thread = key, NC rows)

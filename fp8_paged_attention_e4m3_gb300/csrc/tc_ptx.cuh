@@ -142,6 +142,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// 16 lanes x 256 bits, repeated twice along the columns: thread i writes
+// r[0], r[1] to lane i/4, columns 2(i%4), 2(i%4)+1; r[2], r[3] to lane
+// i/4 + 8, same columns; r[4..7] likewise at columns + 8.
+__device__ __forceinline__ void tmem_st_16x256b_x2(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
 // ------------------------------------------------------------- tcgen05.mma
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (16-byte units), fixed version bits 46..48 = 0b001, swizzle mode
