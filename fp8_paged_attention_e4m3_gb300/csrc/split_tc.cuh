@@ -27,7 +27,10 @@
 //   score MMA warp  : issues tcgen05.mma.kind::f16  S^T[128 x N] = K . Q^T
 //   value MMA warp  : issues tcgen05.mma.kind::f16  O^T[d x N] += V^T . P^T
 //                     (both with A in TMEM and B in shared memory; FP32
-//                     accumulators in TMEM; commits to mbarriers).
+//                     accumulators in TMEM; commits to mbarriers).  One
+//                     lane of each issues the whole chain: a warp-uniform
+//                     loop with an elected issuer was faster alone but
+//                     slower in this kernel.
 //   softmax (8)     : thread = key, half of the N rows each; loads S^T from
 //                     TMEM, applies the causal / partition mask at the
 //                     edges, keeps the FP32 running max per row (raised
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
       tc::mbar_arrive(bar(kKReady));
       tc::mbar_arrive(bar(kKEmpty + st));
     }
-  } else if (warp >= kWVDec) {
+  } else if (warp >= kWVDec && warp < kWKProd) {
     // =============================== V decoders (warp = 32 d per 128-d block)
     const int dq = warp & 3;  // TMEM lane quadrant = d 32*dq.. of each 128-d block
     // ldmatrix rows: threads 0-15 give keys 0-15 of a page, 16-31 the same
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
       tc::mbar_arrive(bar(kVReady + vs));
       tc::mbar_arrive(bar(kVEmpty + st));
     }
-  } else {
+  } else if (warp < kWKDec) {
     // =============================== softmax (thread = key, NC rows)
     const int q = warp & 3, cg = warp >> 2;
     const int col0 = cg * C::NC;
@@ -587,24 +590,40 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
       if (lane == 0) red[warp * 32 + c] = sm;
     }
     alive = alive && tc::mbar_wait(bar(kPvDone), (ntiles - 1) & 1, abort_f, LIM);
-    if (alive) {
-      tc::tc_fence_after();
+    tc::tc_fence_before();
+  }
+
+  // ---- O^T out of TMEM: softmax and decoder warps (4 per lane quadrant)
+  // share the columns once the last value MMA is done
+  if (warp < kWKProd) {
+    tc::named_bar(3, 32 * kWKProd);
+    tc::tc_fence_after();
+    if (*abort_f == 0) {  // every softmax warp saw the last value MMA complete
+      const int q = warp & 3, k4 = warp >> 2;
+      constexpr int NG = C::MH * (N / 8);        // 8-column groups per lane quadrant
+      constexpr int GPW = (NG + 3) / 4;          // groups per warp
       const int64_t slot = ((int64_t)(b * p.Hkv + h) * p.P + part) * p.rows_pad + row0;
+      uint32_t r[GPW][8];
 #pragma unroll
-      for (int mh = 0; mh < C::MH; ++mh) {
+      for (int i = 0; i < GPW; ++i) {
+        const int g = k4 + 4 * i;
+        if (g < NG) {
+          const int mh = g / (N / 8), c8 = g % (N / 8);
+          tc::tmem_ld8(tbase + ((uint32_t)(32 * q) << 16) + C::OCOL + mh * C::SC + c8 * 8, r[i]);
+        }
+      }
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < GPW; ++i) {
+        const int g = k4 + 4 * i;
+        const int mh = g / (N / 8), c8 = g % (N / 8);
         const int d = 128 * mh + 32 * q + lane;
+        if (g < NG && d < D) {
 #pragma unroll
-        for (int c8 = 0; c8 < C::NC / 8; ++c8) {
-          uint32_t r[8];
-          tc::tmem_ld8(tbase + lane_off + C::OCOL + mh * C::SC + col0 + c8 * 8, r);
-          tc::tmem_wait_ld();
-          if (d < D) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              // stored as sum p * dec(V) * 2^-8 (exact scaling): the
-              // combine kernel's convention
-              p.ws_o[(slot + col0 + c8 * 8 + e) * D + d] = __uint_as_float(r[e]) * 0.00390625f;
-            }
+          for (int e = 0; e < 8; ++e) {
+            // stored as sum p * dec(V) * 2^-8 (exact scaling): the
+            // combine kernel's convention
+            p.ws_o[(slot + c8 * 8 + e) * D + d] = __uint_as_float(r[i][e]) * 0.00390625f;
           }
         }
       }
@@ -612,9 +631,12 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     tc::tc_fence_before();
   }
 
-  // ---- wind-down: drain copies and MMAs, free TMEM, publish (max, sum)
+  // ---- wind-down: drain copies and MMAs, free TMEM, publish (max, sum).
+  // A run without an abort has already waited for every load and MMA it
+  // issued (each was consumed); after an abort some may still be in flight.
   __syncthreads();
-  if ((warp == kWKProd || warp == kWVProd) && lane == 0) {
+  const bool drain = *abort_f != 0;
+  if (drain && producer && lane == 0) {
     // every issued load must have landed before the CTA's memory is released
     const int fullb = warp == kWVProd ? kVFull : kKFull;
     const int nslot = warp == kWVProd ? C::NVR : C::NKR;
@@ -622,7 +644,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     for (int s = 0; s < nslot; ++s)
       if (issued[s] > 0) tc::mbar_wait(bar(fullb + s), (issued[s] - 1) & 1, &no_abort, LIM);
   }
-  if ((warp == kWQk || warp == kWPv) && lane == 0 && mma_issued) {
+  if (drain && (warp == kWQk || warp == kWPv) && lane == 0 && mma_issued) {
     const uint32_t db = bar(warp == kWQk ? kDrainQk : kDrainPv);
     tc::mma_commit(db);
     volatile int no_abort = 0;
