@@ -67,15 +67,31 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# the split kernel the default path launches, and the sources that define it
+SPLIT_KERNEL = "vae4::split_tc_kernel<256, 48>"
+SPLIT_SOURCES = ["fp8_paged_attention_e4m3_gb300/csrc/split_tc.cuh",
+                 "fp8_paged_attention_e4m3_gb300/csrc/split_tc.cu",
+                 "fp8_paged_attention_e4m3_gb300/csrc/tc_ptx.cuh",
+                 "fp8_paged_attention_e4m3_gb300/csrc/common.cuh"]
+
+
+def sources_sha256(paths):
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()
+
+
 def kernel_traffic():
     """DRAM bytes per launch of the split kernel from a committed ncu summary,
-    if it was taken on the current kernel source; else None."""
+    if it was taken on this kernel with the current sources; else None."""
     p = os.path.join(ROOT, "profiles", "split_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    h = hashlib.sha256(open(os.path.join(ROOT, d["source"]), "rb").read()).hexdigest()
-    if d.get("source_sha256") != h:
+    if d.get("kernel") != SPLIT_KERNEL or d.get("sources") != SPLIT_SOURCES:
+        return None
+    if d.get("sources_sha256") != sources_sha256(SPLIT_SOURCES):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -317,7 +333,7 @@ def main():
                        "l2": f"inputs rotate over {R} KV pool copies of {pool_bytes >> 20} MiB "
                              f"(> 3x the {l2 >> 20} MiB L2)"},
             "pct_of_hbm_peak": 100.0 * value / world / peak,
-            "roofline": {"bound": "hbm", "kernel": "split (partials)",
+            "roofline": {"bound": "hbm", "kernel": SPLIT_KERNEL,
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                          "traffic": traffic, "split_us_mean": split_mean,
