@@ -7,10 +7,11 @@
 //     w_p = 2^(m_p - M)
 //     out = (sum_p w_p O_p) / (sum_p w_p l_p) * s_V * 2^8
 // all in FP32, rounded once to FP16 (round to nearest even), with a fixed
-// summation order.  This is the
-// single "final combine" of the FP32 max/sum/unnormalised-PV state (PR #524
+// summation order.  It is the one place where the FP32 partition state
+// (max, sum, unnormalised P.V) is reduced, and it reduces in FP32 (PR #524
 // "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32 partials",
-// final status; "FP32 scalar partial storage/reduction", PR #560, Purpose).
+// final status; PR #560 "[Bugfix] Use FP32 state and E4M3 defaults for
+// DFlash2", Purpose).
 // Padding query slots, dead sequences (L == 0) and sequences whose lengths
 // or pages were invalid get zeros.
 #include "common.cuh"

@@ -24,8 +24,8 @@ namespace vae4 {
 // 2^8 is folded into the FP32 scales applied to the accumulators.  The two
 // NaN codes map to the finite 1.875 (480 * 2^-8); a decoded value is never
 // NaN or infinite, so bytes that are later masked out cannot poison a sum.
-// ("exact E4M3 decoder", PR #566 "[Kernel] Finalize the audited TP2 DFlash2
-// 31/29 ms endpoint", Final audit.)
+// (The audited kernel decodes E4M3 exactly: PR #566 "[Kernel] Finalize the
+// audited TP2 DFlash2 31/29 ms endpoint", Final audit.)
 // ---------------------------------------------------------------------------
 constexpr int kDecodeScaleLog2 = -8;
 

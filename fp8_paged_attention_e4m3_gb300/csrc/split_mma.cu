@@ -7,13 +7,12 @@
 // in shared memory, and runs Q.K^T, a masked online softmax and P.V on the
 // tensor cores with the rows (query x group head) as the MMA M dimension.
 // The running max, running sum and unnormalised P.V stay FP32 and are
-// written to the workspace for the combine kernel ("Revision 3 retains FP32
-// max/sum and unnormalized PV until the final combine", PR #524 "[Kernel]
-// [SM70] Add opt-in E4M3 grouped attention with FP32 partials", final
-// status).  Keys are consumed in ascending logical order ("K64 partition
-// order", "ascending PV FMA chain", PR #566, Purpose and Final audit), so
-// the result depends only on logical token positions: moving pages changes
-// no bit.
+// written to the workspace for the combine kernel, which alone merges them
+// (PR #524 "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32
+// partials", final status).  Keys are consumed in ascending logical order,
+// the order the audited kernel fixes for its partitions and its P.V sums
+// (PR #566, Purpose and Final audit), so the result depends only on logical
+// token positions: moving pages changes no bit.
 #include "common.cuh"
 #include "kernels.h"
 #include "verify_attn_e4m3.h"

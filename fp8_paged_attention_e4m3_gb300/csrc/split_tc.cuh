@@ -42,9 +42,8 @@
 // Rows are (query i, group head g) pairs r = i*G + g of KV head h; N of them
 // (<= 64) per CTA form the N dimension of both products (48 for q8 GQA6).
 // The partition's FP32 (max, sum, unnormalised P.V) go to the workspace for
-// the combine kernel ("FP32 max/sum and unnormalized PV until the final
-// combine", PR #524 "[Kernel][SM70] Add opt-in E4M3 grouped attention with
-// FP32 partials", final status).  Keys are visited in ascending logical
+// the combine kernel, the only place they are merged (PR #524 "[Kernel][SM70]
+// Add opt-in E4M3 grouped attention with FP32 partials", final status).  Keys are visited in ascending logical
 // order, so the result does not depend on where pages live.
 //
 // Every mbarrier wait is bounded; on expiry the CTA raises an abort flag,

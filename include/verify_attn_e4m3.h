@@ -11,20 +11,19 @@
  *   For sequence b with L = seq_len[b] cached tokens whose last q = q_len[b]
  *   positions are the draft tokens being verified, query i (0 <= i < q) of q
  *   head hq attends causally to keys 0 .. L-q+i of KV head h = hq / (Hq/Hkv)
- *   (dense q2-8 "GQA6/D256" with "per-query device lengths", PR #524, Scope
- *   and non-duplication; q1 and q16 per PR #560, Purpose and Test Plan):
+ *   (dense q2-8 with 6 q heads per KV head and D = 256, lengths held per
+ *   query on the device: PR #524, Scope and non-duplication; q1 and q16 per
+ *   PR #560, Purpose and Test Plan):
  *
  *     z_j  = softmax_scale * sum_d Q[b,i,hq,d] * dec(K_j[d]) * s_K[h]
  *     out  = sum_j exp(z_j - max z) * dec(V_j[d]) * s_V[h] / sum_j exp(z_j - max z)
  *
- *   dec() is the exact E4M3 (OCP E4M3FN) decode ("exact E4M3 decoder", PR
- *   #566, Final audit); s_K, s_V are per-KV-head FP32 scales ("KV scaling",
- *   PR #560, Test Plan and Results).  The KV storage stays FP8 and the tensor
+ *   dec() is the exact E4M3 (OCP E4M3FN) decode (PR #566, Final audit);
+ *   s_K, s_V are per-KV-head FP32 scales (PR #560, Test Plan and Results).  The KV storage stays FP8 and the tensor
  *   core operands FP16 (PR #560, Purpose).  The context is split into
  *   partitions whose state -- running max, running sum and unnormalised P.V
  *   -- stays FP32 until one final FP32 combine in ascending partition order
- *   (PR #524, final status: "FP32 max/sum and unnormalized PV until the
- *   final combine"; PR #560, Purpose: "FP32 ... partial storage/reduction").
+ *   (PR #524, final status; PR #560, Purpose).
  *
  * Conventions of every entry point:
  *   - All tensor data pointers are DEVICE pointers unless stated otherwise.
@@ -34,8 +33,8 @@
  *     they can be captured in a CUDA graph.  Lengths, block table and scales
  *     are read on the device, so they may change between graph replays.
  *   - A workspace serves one call in flight at a time: use one workspace per
- *     concurrently executing stream ("dtype-separated workspaces", PR #560,
- *     Test Plan and Results).
+ *     concurrently executing stream (the pages keep separate workspaces per
+ *     data type: PR #560, Test Plan and Results).
  *   - Argument errors are returned as negative codes before anything is
  *     launched.  Data errors only visible on the device (block id out of
  *     range, a length beyond capacity, q_len > L, a bounded wait that ran
@@ -53,9 +52,8 @@ extern "C" {
 #endif
 
 /* ABI revision.  A wrapper refuses a library whose revision differs from the
- * one it was written for ("stale libraries fail closed", PR #524, Scope and
- * non-duplication; "Precision revision 4 ... Older binaries cannot silently
- * fall back", PR #560, Purpose). */
+ * one it was written for, so an out-of-date library is refused rather than
+ * used (PR #524, Scope and non-duplication; PR #560, Purpose). */
 #define VAE4_ABI_VERSION 1
 
 /* Same object as cudaStream_t; NULL is the legacy default stream. */
@@ -236,7 +234,7 @@ int verify_attn_e4m3_clear_status(const vae4_tensor *workspace, vae4_stream stre
  * pointer) receives the exponent e with FP16 = dec(b) * 2^e; the kernels
  * fold 2^-e into their FP32 scales.  The NaN codes 0x7F / 0xFF are outside
  * the contract (NaN on the first decoder, a finite pattern on the second).
- * ("exhaustive E4M3 bytes", PR #566, Test Result.)
+ * (The pages test the decoder on every E4M3 byte: PR #566, Test Result.)
  */
 int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2, int32_t flags,
                                   vae4_stream stream);

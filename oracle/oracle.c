@@ -8,22 +8,21 @@
  *
  *  - E4M3 decode, OCP FP8 E4M3FN format (1 sign bit, 4 exponent bits with
  *    bias 7, 3 mantissa bits, no infinities, NaN only at S.1111.111).  The
- *    pages name the format ("exact E4M3 decoder", 1Cat-vLLM PR #566
+ *    pages require an exact decode checked on every byte (1Cat-vLLM PR #566
  *    "[Kernel] Finalize the audited TP2 DFlash2 31/29 ms endpoint", Final
- *    audit; "exhaustive E4M3 bytes", same page, Test Result) but do not define
- *    it; the reading taken is the OCP definition, whose largest finite value
+ *    audit and Test Result) but do not define the format; the reading taken is the OCP definition, whose largest finite value
  *    is the 448 in the per-head scale amax/448.
  *
  *  - Per-KV-head dequantisation x = dec(byte) * s_h, with separate scales for
  *    K and V (PR #560 "[Bugfix] Use FP32 state and E4M3 defaults for
- *    DFlash2", Test Plan and Results: "KV scaling").
+ *    DFlash2", Test Plan and Results).
  *
  *  - Scaled-dot-product attention per (sequence b, query i, q head hq) in
  *    FP64: q head hq reads KV head hq / (Hq/Hkv) (GQA6/D256 grouping, PR #524
  *    "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32 partials",
  *    Scope and non-duplication).  The q_len queries occupy the last q_len
  *    positions of the L cached tokens, so query i sees keys 0 .. L-q_len+i
- *    ("per-query device lengths", same section).  Token j of sequence b lives
+ *    (lengths per query, same section).  Token j of sequence b lives
  *    in physical page block_table[b][j / page] at slot j % page.
  *
  *  - Two evaluation modes.  Direct: two passes (maximum, then exponentials
