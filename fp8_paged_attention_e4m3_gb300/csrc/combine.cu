@@ -38,9 +38,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   __shared__ float red[kCombineThreads / 32];
   __shared__ float4 accs[kGroups][kLanes];
 
-  // wait until the split kernel's partials are complete and visible
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
-
   const int nd = p.D / 64;  // d slices per row
   const int r = blockIdx.x / nd, dsl = blockIdx.x - r * nd;
   const int h = blockIdx.y, b = blockIdx.z;
@@ -50,8 +47,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   __half *out = static_cast<__half *>(p.out) + (int64_t)b * p.o_sb + (int64_t)i * p.o_si +
                 (int64_t)(h * p.G + g) * p.o_sh + d0;
 
+  // lengths are inputs of the step, not results of the split kernel: read
+  // them before waiting for it
   const int L = p.seq[(int64_t)b * p.seq_sb];
   const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
+  // wait until the split kernel's partials are complete and visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql;
   const int nP = dead ? 0 : (L + p.T - 1) / p.T;
 
@@ -60,6 +61,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   const int64_t pstride = (int64_t)p.rows_pad;  // rows per partition
   const float *ml = p.ws_ml + (int64_t)(b * p.Hkv + h) * p.P * pstride * 2 + r * 2;
   const float kNegInf = -__int_as_float(0x7f800000);
+
+  // the first kPre P.V partials of this thread's group are requested now,
+  // together with the (m, l) pairs, so both L2 round trips overlap
+  const int l4 = tid % kLanes, grp = tid / kLanes;
+  const float *o = p.ws_o + (int64_t)(b * p.Hkv + h) * p.P * pstride * p.D + (int64_t)r * p.D +
+                   d0 + 4 * l4;
+  const int64_t ostride = pstride * p.D;
+  constexpr int kPre = 10;  // covers 160 partitions
+  float4 pre[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int q = grp + k * kGroups;
+    pre[k] = q < nP ? __ldcg(reinterpret_cast<const float4 *>(o + q * ostride))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 
   // ---- pass 1: (m_p, l_p), maximum over partitions with l_p > 0
   float mx = kNegInf;
@@ -96,14 +112,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 #pragma unroll
   for (int k = 0; k < kCombineThreads / 32; ++k) Lam += red[k];
 
-  // ---- pass 3: sum of w_p * O_p over this slice, per group, then over groups
-  const int l4 = tid % kLanes, grp = tid / kLanes;
-  const float *o = p.ws_o + (int64_t)(b * p.Hkv + h) * p.P * pstride * p.D + (int64_t)r * p.D +
-                   d0 + 4 * l4;
-  const int64_t ostride = pstride * p.D;
+  // ---- pass 3: sum of w_p * O_p over this slice, per group (ascending p),
+  // then over groups
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int q = grp; q < nP; q += kGroups) {
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int q = grp + k * kGroups;
+    if (q < nP) {
+      const float w = wm[q];
+      acc.x += w * pre[k].x;
+      acc.y += w * pre[k].y;
+      acc.z += w * pre[k].z;
+      acc.w += w * pre[k].w;
+    }
+  }
+#pragma unroll 4
+  for (int q = grp + kPre * kGroups; q < nP; q += kGroups) {
     const float w = wm[q];
     const float4 v = __ldcg(reinterpret_cast<const float4 *>(o + q * ostride));
     acc.x += w * v.x;

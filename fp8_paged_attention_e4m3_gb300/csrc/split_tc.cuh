@@ -229,6 +229,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   tc::tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(gSm + kSmTslot);
   const long long LIM = a.wait_limit;
+  // the combine kernel may be placed on SMs as they free up; it waits for
+  // this grid's completion before reading any partial
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   constexpr int kSetup = C::NTHREADS - 64;  // every thread but the producers
   if (!producer) {
     const int st_id = tid < 32 * kWKProd ? tid : tid - 64;
