@@ -53,6 +53,23 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(values, device):
+    """Max over ranks of per-rank timings (one all-reduce); identity at N=1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def aggregate_gbs(world, kv_bytes_per_rank, ms_per_step):
+    """Whole-job throughput: the KV bytes all ranks read, over the slowest
+    rank's step time (weak scaling: each rank holds a full replica)."""
+    return world * kv_bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def workload_desc(w):
     s = w.spec
     return (f"{s.name}: B{s.B} q{int(w.q_len[0])} Hq{s.Hq} Hkv{s.Hkv} D{s.D} "
@@ -302,14 +319,10 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     t_step = total_ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_step, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, e2e_ms = float(t[0]), float(t[1])
+    t_step, e2e_ms, split_mean_us = reduce_max([t_step, e2e_ms, split_mean_us], dev)
     kv_bytes = w.kv_bytes
-    value = world * kv_bytes / (t_step * 1e-3) / 1e9
-    e2e_value = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
+    value = aggregate_gbs(world, kv_bytes, t_step)
+    e2e_value = aggregate_gbs(world, kv_bytes, e2e_ms)
 
     if rank == 0:
         peak, peak_kind = peaks()
