@@ -291,8 +291,31 @@ def main():
     time.sleep(0.3)  # let the sampler start before the timed region
     total_ms = timed(g_step)
     split_total_ms = timed(g_split)
+    # ---- the step against the gather floor: the streaming-read kernel reads
+    # exactly the step's KV bytes with plain loads and no compute.  Blocks of
+    # KB launches, graph-replayed, A/B-interleaved (ABBA) after warm-up
+    # replays; per-launch median and p90 of each.
+    KB, NPAIR = 8, 25
+    g_a, g_b = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_a, stream=stream):
+        for k in range(KB):
+            vae4.verify(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
+    with torch.cuda.graph(g_b, stream=stream):
+        for k in range(KB):
+            vae4.verify_attn_e4m3_kv_read(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
+    for _ in range(20):
+        with torch.cuda.stream(stream):
+            g_a.replay()
+            g_b.replay()
+    torch.cuda.synchronize()
+    samp = {"a": [], "b": []}
+    for i in range(NPAIR):
+        for tag in (("a", "b") if i % 2 == 0 else ("b", "a")):
+            samp[tag].append(timed(g_a if tag == "a" else g_b) * 1e3 / KB)
     clocks = sampler.stop()
     split_mean_us = split_total_ms * 1e3 / args.steps
+    step_med, step_p90 = float(np.median(samp["a"])), float(np.percentile(samp["a"], 90))
+    floor_med, floor_p90 = float(np.median(samp["b"])), float(np.percentile(samp["b"], 90))
     assert vae4.read_status(ws) == 0
     gpu_launches = 2 * args.steps
     stream = torch.cuda.current_stream()
@@ -357,6 +380,13 @@ def main():
                              "seconds": cpu_s},
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gather_floor": {
+                "kernel": "verify_attn_e4m3_kv_read (plain 16-byte loads of the step's KV bytes)",
+                "us_median": floor_med, "us_p90": floor_p90,
+                "gbs_median": kv_bytes / (floor_med * 1e-6) / 1e9,
+                "step_us_median": step_med, "step_us_p90": step_p90,
+                "step_over_floor": step_med / floor_med,
+                "samples": f"{NPAIR} ABBA pairs of {KB}-launch graph replays after 20 warm-up pairs"},
             "gpu_launches": gpu_launches,
             "clocks": clocks,
             "gpu": props.name,

@@ -37,7 +37,7 @@ EXPORTS = (
     "verify_attn_e4m3_workspace_bytes", "verify_attn_e4m3_abi_version",
     "verify_attn_e4m3_strerror", "verify_attn_e4m3_read_status",
     "verify_attn_e4m3_clear_status", "verify_attn_e4m3_decode_table",
-    "verify_attn_e4m3_noalloc",
+    "verify_attn_e4m3_noalloc", "verify_attn_e4m3_kv_read",
 )
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -91,7 +91,7 @@ def load(build_if_stale: bool = True):
             getattr(lib, name).argtypes = [P] * 7 + [ctypes.c_void_p]
             getattr(lib, name).restype = ctypes.c_int
         for name in ("verify_attn_e4m3_ex", "verify_attn_e4m3_partials",
-                     "verify_attn_e4m3_combine"):
+                     "verify_attn_e4m3_combine", "verify_attn_e4m3_kv_read"):
             getattr(lib, name).argtypes = [P] * 7 + [ctypes.c_void_p, ctypes.POINTER(Options)]
             getattr(lib, name).restype = ctypes.c_int
         lib.verify_attn_e4m3_plan.argtypes = [ctypes.c_int] * 5 + [
@@ -215,6 +215,12 @@ def verify_attn_e4m3_partials(*args, **kw):
 def verify_attn_e4m3_combine(*args, **kw):
     """Combine stage only (see the header)."""
     return _stage("verify_attn_e4m3_combine", *args, **kw)
+
+
+def verify_attn_e4m3_kv_read(*args, **kw):
+    """Streaming read of the step's KV bytes, no compute (see the header):
+    the gather floor the step is measured against."""
+    return _stage("verify_attn_e4m3_kv_read", *args, **kw)
 
 
 def verify_attn_e4m3_noalloc(q, kv_pages, block_table, seq_lens, kv_scales, out, *,

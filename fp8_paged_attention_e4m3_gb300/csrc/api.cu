@@ -101,6 +101,7 @@ struct Prepared {
   int64_t ws_needed;
   bool empty;
   bool warp_mma;
+  int num_sms;
 };
 
 // SM cycles a pipeline wait of the tcgen05 kernel may take before the CTA
@@ -199,6 +200,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   pr->ws_needed = lay.total;
   pr->empty = (B == 0);
   pr->warp_mma = (o.flags & VAE4_FLAG_WARP_MMA) != 0;
+  pr->num_sms = sms;
   if (B > 0 && ws->shape[0] < lay.total) return VAE4_ERR_WORKSPACE;
   if (!q->data || !kv->data || !bt->data || !seq->data || !sc->data || !out->data ||
       !ws->data) {
@@ -314,6 +316,21 @@ int verify_attn_e4m3_combine(const vae4_tensor *q, const vae4_tensor *kv_pages,
   if (rc) return rc;
   if (pr.empty) return VAE4_OK;
   if (vae4::launch_combine(pr.cp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+int verify_attn_e4m3_kv_read(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                             const vae4_tensor *block_table, const vae4_tensor *seq_lens,
+                             const vae4_tensor *kv_scales, const vae4_tensor *out,
+                             const vae4_tensor *workspace, vae4_stream stream,
+                             const vae4_options *opt) {
+  Prepared pr;
+  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  if (rc) return rc;
+  if (pr.empty) return VAE4_OK;
+  if (vae4::launch_kv_read(pr.sp, pr.num_sms, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
     return VAE4_ERR_CUDA;
   return VAE4_OK;
 }

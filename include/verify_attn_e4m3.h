@@ -183,6 +183,27 @@ int verify_attn_e4m3_combine(const vae4_tensor *q, const vae4_tensor *kv_pages,
                              const vae4_options *opt);
 
 /*
+ * Measurement helper (not a step of the method): reads every KV byte that
+ * verify_attn_e4m3 with the same arguments reads -- K and V of tokens
+ * 0 .. L-1 of every (sequence, KV head), through the block table, in the
+ * same page order -- with plain 16-byte loads and no arithmetic.  Its time
+ * is the floor of the step's page gather on the running GPU; the pages time
+ * their kernels in graph-replayed A/B blocks against a reference in the same
+ * way (PR #560 "[Bugfix] Use FP32 state and E4M3 defaults for DFlash2", Test
+ * Plan and Results).  Same arguments and validation as verify_attn_e4m3_ex;
+ * q and out are validated but not read or written.  XORs every 32-bit word
+ * it reads into the word at workspace byte 128 (a checksum: zero that word
+ * first to read it; the status word at byte 0 is not touched).  Pages with invalid ids and sequences with invalid lengths are
+ * skipped without a status bit.
+ */
+int verify_attn_e4m3_kv_read(const vae4_tensor *q, const vae4_tensor *kv_pages,
+                             const vae4_tensor *block_table,
+                             const vae4_tensor *seq_lens,
+                             const vae4_tensor *kv_scales, const vae4_tensor *out,
+                             const vae4_tensor *workspace, vae4_stream stream,
+                             const vae4_options *opt);
+
+/*
  * verify_attn_e4m3_plan -- the split-K partition plan (host only, no CUDA).
  * Partition p of every sequence covers tokens [p*T, min((p+1)*T, L)); the
  * launch has P = ceil(max_seq_len / T) partitions per (sequence, KV head).
