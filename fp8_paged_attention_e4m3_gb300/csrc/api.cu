@@ -138,7 +138,8 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
       kv->shape[2] < 1)
     return VAE4_ERR_SHAPE;
   const int64_t n_pages = kv->shape[0], Hkv = kv->shape[2], page = kv->shape[3];
-  if (page != 16 && page != 32 && page != 64 && page != 128) return VAE4_ERR_UNSUPPORTED;
+  // any multiple of 16 tokens: the kernels move 16-key page slices
+  if (page < 16 || page % 16 != 0 || page > 65536) return VAE4_ERR_UNSUPPORTED;
   if (kv->stride[4] != 1 || kv->stride[3] != D || kv->stride[2] != page * D ||
       kv->stride[1] != Hkv * page * D || kv->stride[0] != 2 * Hkv * page * D)
     return VAE4_ERR_STRIDE;

@@ -172,10 +172,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   // its latency overlaps the set-up.  Lane l holds logical page lp_base + l
   // (cur) and lp_base + 32 + l (nxt); entries past the row are -1, entries
   // past the sequence are loaded but never used.
-  const int page_shift = __ffs(p.page) - 1;
   const int32_t *btb = p.bt + (int64_t)b * p.bt_sb;
   auto fetch = [&](int lp) -> int { return lp < p.max_pages ? __ldg(btb + lp) : -1; };
-  int lp_base = (part * p.T) >> page_shift;
+  int lp_base = (part * p.T) / p.page;  // any page size that is a multiple of 16
   int cur = -1, nxt = -1;
   if (producer) {
     cur = fetch(lp_base + lane);
@@ -276,7 +275,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const int key0 = k0 + 64 * t + 16 * g;
-        const int lp = key0 >> page_shift;
+        const int lp = key0 / p.page;  // a 16-key box never crosses a page
         while (lp >= lp_base + 32) {  // advance the register window (warp-uniform)
           cur = nxt;
           lp_base += 32;
@@ -288,7 +287,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
           if (key0 < k1) {
             if (phys >= 0 && phys < p.n_pages)
               row = (int)(((int64_t)phys * 2 * p.Hkv + (isv ? p.Hkv : 0) + h) * p.page +
-                          (key0 - (lp << page_shift)));
+                          (key0 - lp * p.page));
             else
               *bad_f = 1;
           }

@@ -126,12 +126,15 @@ enum vae4_error {
  *              i of sequence b is a query only if i < q_len[b]; the other
  *              slots are padding and are never read.
  *  kv_pages    U8 [n_pages][2][Hkv][page][D], contiguous; index 0 of dim 1
- *              is K, 1 is V; page in {16, 32, 64, 128} tokens; base 16-byte
- *              aligned.  Each (page, K|V, head) slice of page*D bytes is one
- *              contiguous 16-byte-aligned block.
+ *              is K, 1 is V; page = any multiple of 16 tokens up to 65536
+ *              (the pages run 16-token pages and 848- to 3456-token blocks:
+ *              PR #560, Purpose and Test Plan and Results; PR #524, AI
+ *              review); base 16-byte aligned.  Each (page, K|V, head) slice
+ *              of page*D bytes is one contiguous 16-byte-aligned block.
  *  block_table I32 [B][max_pages], stride[1] == 1: logical page j of
- *              sequence b lives in physical page block_table[b][j].  Only
- *              the first ceil(L/page) entries of a row are read.
+ *              sequence b lives in physical page block_table[b][j].  The ids
+ *              of the first ceil(L/page) entries of a row are used; up to 64
+ *              entries beyond them (within the row) may be read and ignored.
  *  seq_lens    I32 [B] (L; q_len = Qmax for every sequence) or I32 [B][2]
  *              with stride[1] == 1 holding (L, q_len).  L counts the q tail.
  *              L == 0 marks a dead sequence (all-zero output, no status bit).

@@ -139,6 +139,11 @@ def _call(lib, a, opt=None):
     (dict(q=_t(vae4.VAE4_F16, [1, 8, 6, 256], [12288, 1536, 256, 2])), -4),
     (dict(q=_t(vae4.VAE4_F16, [1, 8, 6, 256], [12290, 1536, 256, 1])), -4),
     (dict(kv=_t(vae4.VAE4_U8, [80, 2, 1, 24, 256])), -6),           # page 24
+    (dict(kv=_t(vae4.VAE4_U8, [80, 2, 1, 40, 256])), -6),           # page 40
+    # pages that are multiples of 16 pass the page check (and then fail on
+    # the head grouping, 6 q heads over 4 KV heads)
+    (dict(kv=_t(vae4.VAE4_U8, [80, 2, 4, 48, 256])), -7),           # page 48
+    (dict(kv=_t(vae4.VAE4_U8, [8, 2, 4, 3296, 256])), -7),          # page 3296
     (dict(kv=_t(vae4.VAE4_U8, [80, 2, 4, 16, 256])), -7),           # 6 % 4
     (dict(kv=_t(vae4.VAE4_U8, [80, 2, 1, 16, 256], data=FAKE + 8)), -5),
     (dict(kv=_t(vae4.VAE4_U8, [80, 2, 1, 16, 256], [8448, 4224, 4224, 264, 1])), -4),

@@ -118,6 +118,21 @@ SMALL = [
          pad_q_nan=True, partition_tokens=256),
 ]
 
+# Large and odd page sizes (multiples of 16 tokens): the pages run 1728-,
+# 3296- and 3456-token blocks and an 848-token block (PR #560, Purpose and
+# Test Plan and Results; PR #524, AI review).  Partitions cut pages in the
+# middle.
+LARGE_PAGES = [
+    dict(B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[5000, 1729], q_lens=[8, 8], seed=52,
+         page=1728, partition_tokens=1024),
+    dict(B=1, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[7000], q_lens=[8], seed=53, page=3296),
+    dict(B=1, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[2000], q_lens=[8], seed=54, page=848,
+         partition_tokens=400),
+    dict(B=2, Qmax=4, Hq=4, Hkv=2, D=128, seq_lens=[1000, 333], q_lens=[4, 2], seed=55,
+         page=48, partition_tokens=176),
+    dict(B=1, Qmax=8, Hq=2, Hkv=1, D=64, seq_lens=[3500], q_lens=[8], seed=56, page=3456),
+]
+
 
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.get("name", str(c.get("seed"))))
 def test_parity_small(cfg):
@@ -128,6 +143,13 @@ def test_parity_small(cfg):
         cfg.pop("name", None)
         w = W.custom("small", **cfg)
     check_full(w)
+
+
+@pytest.mark.parametrize("cfg", LARGE_PAGES, ids=lambda c: f"page{c['page']}")
+@pytest.mark.parametrize("flags", [0, 1], ids=["tcgen05-path", "mma-sync-path"])
+def test_parity_large_pages(cfg, flags):
+    w = W.custom("pages", **cfg)
+    check_full(w, flags=flags)
 
 
 @pytest.mark.parametrize("cfg", [SMALL[0], SMALL[1], SMALL[4], SMALL[11]],

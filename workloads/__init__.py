@@ -32,7 +32,13 @@ import numpy as np
 
 E4M3_MAX = np.float32(448.0)
 PAGE = 16
-GEN_PAGES = 256      # pages per random-stream block (part of the recipe)
+GEN_PAGES = 256      # 16-token pages per random-stream block (part of the recipe)
+
+
+def gen_pages(page: int) -> int:
+    """Pages per random-stream block: 4096 tokens' worth (256 pages of 16
+    tokens; fewer, larger pages for larger page sizes, at least one)."""
+    return max(1, GEN_PAGES * 16 // page)
 _CHUNK_BLOCKS = 8    # blocks per processing chunk (memory only)
 
 
@@ -161,9 +167,9 @@ def _rng(*key) -> np.random.Generator:
 
 def _kv_block(seed: int, kv_sel: int, h: int, block: int, page: int, D: int,
               outliers: bool) -> np.ndarray:
-    """fp32 K or V values of pages [block*GEN_PAGES, (block+1)*GEN_PAGES)."""
+    """fp32 K or V values of pages [block*gp, (block+1)*gp), gp = gen_pages(page)."""
     rng = _rng(seed, 1000 + kv_sel, h, block)
-    shape = (GEN_PAGES, page, D)
+    shape = (gen_pages(page), page, D)
     x = rng.standard_normal(shape, dtype=np.float32)
     if outliers:
         # one uniform draw: u < 1e-3 marks an outlier, u < 5e-4 makes it negative
@@ -175,9 +181,9 @@ def _kv_block(seed: int, kv_sel: int, h: int, block: int, page: int, D: int,
 
 
 def _kv_chunk(seed, kv_sel, h, chunk, n_pages, page, D, outliers):
-    """Pages [chunk*_CHUNK_BLOCKS*GEN_PAGES, ...) of the pool, n_pages of them."""
+    """Pages [chunk*_CHUNK_BLOCKS*gp, ...) of the pool, n_pages of them."""
     b0 = chunk * _CHUNK_BLOCKS
-    nb = -(-n_pages // GEN_PAGES)
+    nb = -(-n_pages // gen_pages(page))
     x = np.concatenate([_kv_block(seed, kv_sel, h, b0 + k, page, D, outliers)
                         for k in range(nb)])
     return x[:n_pages]
@@ -210,7 +216,7 @@ def generate(s: Spec | str) -> Workload:
     # K/V: per (K|V, head) two passes over chunks: amax, then quantise
     kv = np.empty((n_pages, 2, Hkv, page, D), dtype=np.uint8)
     scales = np.empty((Hkv, 2), dtype=np.float32)
-    chunk_pages = _CHUNK_BLOCKS * GEN_PAGES
+    chunk_pages = _CHUNK_BLOCKS * gen_pages(page)
     n_chunks = -(-n_pages // chunk_pages)
     for sel in range(2):
         for h in range(Hkv):
