@@ -17,6 +17,7 @@ ABI_VERSION = 1
 VAE4_U8, VAE4_I32, VAE4_F16, VAE4_F32 = 1, 2, 3, 4
 
 FLAG_WARP_MMA = 0x1
+FLAG_KV_E5M2 = 0x2
 
 STATUS_BAD_BLOCK = 0x1
 STATUS_BAD_LENGTH = 0x2

@@ -120,7 +120,9 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   vae4_options o;
   memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
-  if ((o.flags & ~VAE4_FLAG_WARP_MMA) != 0) return VAE4_ERR_OPTIONS;
+  if ((o.flags & ~(VAE4_FLAG_WARP_MMA | VAE4_FLAG_KV_E5M2)) != 0) return VAE4_ERR_OPTIONS;
+  if ((o.flags & VAE4_FLAG_WARP_MMA) && (o.flags & VAE4_FLAG_KV_E5M2))
+    return VAE4_ERR_UNSUPPORTED;
 
   int rc = check_qo(q);
   if (rc) return rc;
@@ -247,6 +249,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   s.P = P;
   s.capacity = (int32_t)cap;
   s.sm_scale = sm_scale;
+  s.kv_e5m2 = (o.flags & VAE4_FLAG_KV_E5M2) ? 1 : 0;
 
   CombineParams &c = pr->cp;
   memset(&c, 0, sizeof(c));
@@ -420,10 +423,12 @@ int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2, int32_t fl
                                   vae4_stream stream) {
   if (!dev_out || !scale_log2) return VAE4_ERR_NULL;
   if (!al16(dev_out)) return VAE4_ERR_MISALIGNED;
-  if ((flags & ~VAE4_FLAG_WARP_MMA) != 0) return VAE4_ERR_OPTIONS;
+  if ((flags & ~(VAE4_FLAG_WARP_MMA | VAE4_FLAG_KV_E5M2)) != 0) return VAE4_ERR_OPTIONS;
+  if ((flags & VAE4_FLAG_WARP_MMA) && (flags & VAE4_FLAG_KV_E5M2)) return VAE4_ERR_UNSUPPORTED;
   const bool integer_path = (flags & VAE4_FLAG_WARP_MMA) != 0;
+  const bool e5m2 = (flags & VAE4_FLAG_KV_E5M2) != 0;
   *scale_log2 = integer_path ? -8 : 0;
-  if (vae4::launch_decode_table(static_cast<uint16_t *>(dev_out), integer_path,
+  if (vae4::launch_decode_table(static_cast<uint16_t *>(dev_out), integer_path, e5m2,
                                 reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return VAE4_ERR_CUDA;
   return VAE4_OK;

@@ -158,15 +158,19 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   *reinterpret_cast<uint2 *>(out + 4 * l4) = res;
 }
 
-__global__ void decode_table_kernel(uint16_t *out, bool integer_path) {
+__global__ void decode_table_kernel(uint16_t *out, bool integer_path, bool e5m2) {
   const int t = threadIdx.x;  // 64 threads x 4 codes
   const uint32_t w = (uint32_t)(4 * t) | (uint32_t)(4 * t + 1) << 8 | (uint32_t)(4 * t + 2) << 16 |
                      (uint32_t)(4 * t + 3) << 24;
   uint32_t lo, hi;
-  if (integer_path)
+  if (e5m2) {
+    lo = fp8x2_to_f16x2<true>(w);
+    hi = fp8x2_to_f16x2<true>(w >> 16);
+  } else if (integer_path) {
     e4m3x4_to_f16x4(w, lo, hi);
-  else
+  } else {
     e4m3x4_to_f16x4_hw(w, lo, hi);
+  }
   out[4 * t + 0] = (uint16_t)(lo & 0xFFFFu);
   out[4 * t + 1] = (uint16_t)(lo >> 16);
   out[4 * t + 2] = (uint16_t)(hi & 0xFFFFu);
@@ -196,8 +200,9 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
-cudaError_t launch_decode_table(uint16_t *out, bool integer_path, cudaStream_t stream) {
-  decode_table_kernel<<<1, 64, 0, stream>>>(out, integer_path);
+cudaError_t launch_decode_table(uint16_t *out, bool integer_path, bool e5m2,
+                                cudaStream_t stream) {
+  decode_table_kernel<<<1, 64, 0, stream>>>(out, integer_path, e5m2);
   return cudaGetLastError();
 }
 

@@ -62,6 +62,18 @@ __device__ __forceinline__ void e4m3x16_to_f16x16_hw(const uint4 &raw, uint4 &h0
   e4m3x4_to_f16x4_hw(raw.w, h1.z, h1.w);
 }
 
+// Two FP8 bytes (byte 0 -> low half) -> f16x2, exact for every finite code.
+// E4M3 through the hardware converter; an E5M2 byte is the high byte of the
+// FP16 with the same value (same sign, 5-bit exponent with bias 15, the two
+// mantissa bits on top of FP16's ten), so it is a byte move.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_bytes) {
+  if constexpr (E5M2)
+    return __byte_perm(two_bytes, 0u, 0x1404);  // (b1 << 24) | (b0 << 8)
+  else
+    return cvt_e4m3x2(two_bytes);
+}
+
 // 16 bytes -> 16 halves (two uint4 of f16x2).
 __device__ __forceinline__ void e4m3x16_to_f16x16(const uint4 &raw, uint4 &h0,
                                                   uint4 &h1) {

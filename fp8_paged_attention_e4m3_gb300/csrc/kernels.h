@@ -26,6 +26,7 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 cudaError_t launch_kv_read(const SplitParams &p, int num_sms, cudaStream_t stream);
 
 // Decode-table test hook.
-cudaError_t launch_decode_table(uint16_t *out, bool integer_path, cudaStream_t stream);
+cudaError_t launch_decode_table(uint16_t *out, bool integer_path, bool e5m2,
+                                cudaStream_t stream);
 
 }  // namespace vae4

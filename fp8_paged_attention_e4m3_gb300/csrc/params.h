@@ -29,6 +29,7 @@ struct SplitParams {
   int32_t P;            // partitions per (b, h)
   int32_t capacity;     // launch capacity (tokens)
   float sm_scale;       // softmax scale
+  int32_t kv_e5m2;      // 1: the KV bytes are E5M2, 0: E4M3
 };
 
 // The combine kernel's parameters.

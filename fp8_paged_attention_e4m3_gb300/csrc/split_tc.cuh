@@ -54,6 +54,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "params.h"
 #include "tc_ptx.cuh"
@@ -351,95 +353,112 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     const int kh = dq >> 1;               // half-tile of the 128-key tile
     const int kk = 32 * (dq & 1) + lane;  // key within the half-tile
     const uint32_t lane_off = (uint32_t)(32 * dq) << 16;
-    for (int j = 0; j < ntiles; ++j) {
-      const int t = 2 * j + kh;
-      // K -> TMEM: column c holds d = 2c (low half), 2c+1 (high half).
-      // Wait for the previous tile's score MMA first: it proves every
-      // earlier K half-tile (in particular this slot's previous use, t -
-      // NKR <= t - 2) has landed and been read, so the parity wait on the
-      // slot below cannot match an older phase when pairs share slots.
-      const int st = t % C::NKR;
-      if (j > 0 && !tc::mbar_wait(bar(kKFree), (j - 1) & 1, abort_f, LIM)) break;
-      if (!tc::mbar_wait(bar(kKFull + st), (t / C::NKR) & 1, abort_f, LIM)) break;
-      tc::tc_fence_after();
-      const uint8_t *rawK = gKR + st * C::RSLOT;
+    // one copy of the loop per KV format (the run takes one of them)
+    auto decode_k = [&](auto e5m2) {
+      constexpr bool E5 = decltype(e5m2)::value;
+      for (int j = 0; j < ntiles; ++j) {
+        const int t = 2 * j + kh;
+        // K -> TMEM: column c holds d = 2c (low half), 2c+1 (high half).
+        // Wait for the previous tile's score MMA first: it proves every
+        // earlier K half-tile (in particular this slot's previous use, t -
+        // NKR <= t - 2) has landed and been read, so the parity wait on the
+        // slot below cannot match an older phase when pairs share slots.
+        const int st = t % C::NKR;
+        if (j > 0 && !tc::mbar_wait(bar(kKFree), (j - 1) & 1, abort_f, LIM)) break;
+        if (!tc::mbar_wait(bar(kKFull + st), (t / C::NKR) & 1, abort_f, LIM)) break;
+        tc::tc_fence_after();
+        const uint8_t *rawK = gKR + st * C::RSLOT;
 #pragma unroll
-      for (int grp = 0; grp < D / 64; ++grp) {
-        uint32_t r[32];
+        for (int grp = 0; grp < D / 64; ++grp) {
+          uint32_t r[32];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int c = grp * 4 + q4;  // 16-byte chunk of the key row
-          const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
-          const uint32_t off = (uint32_t)((kk & 15) * C::IB + cc * 16);
-          const uint4 w = *reinterpret_cast<const uint4 *>(
-              rawK + (kk >> 4) * (16 * D) + dh * (16 * C::IB) +
-              (off ^ (((off >> 7) & C::SMASK) << 4)));
-          e4m3x4_to_f16x4_hw(w.x, r[q4 * 8 + 0], r[q4 * 8 + 1]);
-          e4m3x4_to_f16x4_hw(w.y, r[q4 * 8 + 2], r[q4 * 8 + 3]);
-          e4m3x4_to_f16x4_hw(w.z, r[q4 * 8 + 4], r[q4 * 8 + 5]);
-          e4m3x4_to_f16x4_hw(w.w, r[q4 * 8 + 6], r[q4 * 8 + 7]);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int c = grp * 4 + q4;  // 16-byte chunk of the key row
+            const int dh = (c * 16) / C::IB, cc = ((c * 16) % C::IB) >> 4;
+            const uint32_t off = (uint32_t)((kk & 15) * C::IB + cc * 16);
+            const uint4 w = *reinterpret_cast<const uint4 *>(
+                rawK + (kk >> 4) * (16 * D) + dh * (16 * C::IB) +
+                (off ^ (((off >> 7) & C::SMASK) << 4)));
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              r[q4 * 8 + 2 * e] = fp8x2_to_f16x2<E5>(wv[e]);
+              r[q4 * 8 + 2 * e + 1] = fp8x2_to_f16x2<E5>(wv[e] >> 16);
+            }
+          }
+          const uint32_t (&r0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[0]);
+          const uint32_t (&r1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[16]);
+          tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32, r0);
+          tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32 + 16, r1);
         }
-        const uint32_t (&r0)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[0]);
-        const uint32_t (&r1)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&r[16]);
-        tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32, r0);
-        tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32 + 16, r1);
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(bar(kKReady));
+        tc::mbar_arrive(bar(kKEmpty + st));
       }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      tc::mbar_arrive(bar(kKReady));
-      tc::mbar_arrive(bar(kKEmpty + st));
-    }
+    };
+    if (p.kv_e5m2)
+      decode_k(std::true_type{});
+    else
+      decode_k(std::false_type{});
   } else if (warp >= kWVDec && warp < kWKProd) {
     // =============================== V decoders (warp = 32 d per 128-d block)
     const int dq = warp & 3;  // TMEM lane quadrant = d 32*dq.. of each 128-d block
     // ldmatrix rows: threads 0-15 give keys 0-15 of a page, 16-31 the same
     // rows of the next page (two 16 x 16 byte matrices per load)
     const int pr = lane & 15, pg = lane >> 4;
-    for (int t = 0; t < nhalf; ++t) {
-      // V -> V^T in TMEM (lane = d, column c = keys 2c, 2c+1).  Wait for
-      // the value MMA that last read the V^T slot first: it proves
-      // half-tiles up to t - NVF >= t - NVR were decoded, i.e. this raw
-      // slot's previous use is complete, so the parity wait below is
-      // unambiguous.
-      const int st = t % C::NVR, vs = t % C::NVF;
-      if (t >= C::NVF && !tc::mbar_wait(bar(kVFree + vs), ((t / C::NVF) - 1) & 1, abort_f, LIM))
-        break;
-      if (!tc::mbar_wait(bar(kVFull + st), (t / C::NVR) & 1, abort_f, LIM)) break;
-      tc::tc_fence_after();
-      const uint32_t rawV = sVR + st * C::RSLOT;
+    auto decode_v = [&](auto e5m2) {
+      constexpr bool E5 = decltype(e5m2)::value;
+      for (int t = 0; t < nhalf; ++t) {
+        // V -> V^T in TMEM (lane = d, column c = keys 2c, 2c+1).  Wait for
+        // the value MMA that last read the V^T slot first: it proves
+        // half-tiles up to t - NVF >= t - NVR were decoded, i.e. this raw
+        // slot's previous use is complete, so the parity wait below is
+        // unambiguous.
+        const int st = t % C::NVR, vs = t % C::NVF;
+        if (t >= C::NVF && !tc::mbar_wait(bar(kVFree + vs), ((t / C::NVF) - 1) & 1, abort_f, LIM))
+          break;
+        if (!tc::mbar_wait(bar(kVFull + st), (t / C::NVR) & 1, abort_f, LIM)) break;
+        tc::tc_fence_after();
+        const uint32_t rawV = sVR + st * C::RSLOT;
 #pragma unroll
-      for (int mh = 0; mh < C::MH; ++mh) {
+        for (int mh = 0; mh < C::MH; ++mh) {
 #pragma unroll
-        for (int dc = 0; dc < 2; ++dc) {
-          const int dch = 128 * mh + 32 * dq + 16 * dc;  // first d of the 16-d chunk
-          if (dch < D) {
-            const int dh = dch / C::IB, cc = (dch % C::IB) >> 4;
-            const uint32_t off = (uint32_t)(pr * C::IB + cc * 16);
-            const uint32_t src = rawV + dh * (16 * C::IB) + (off ^ (((off >> 7) & C::SMASK) << 4));
+          for (int dc = 0; dc < 2; ++dc) {
+            const int dch = 128 * mh + 32 * dq + 16 * dc;  // first d of the 16-d chunk
+            if (dch < D) {
+              const int dh = dch / C::IB, cc = (dch % C::IB) >> 4;
+              const uint32_t off = (uint32_t)(pr * C::IB + cc * 16);
+              const uint32_t src = rawV + dh * (16 * C::IB) + (off ^ (((off >> 7) & C::SMASK) << 4));
 #pragma unroll
-            for (int kp = 0; kp < 2; ++kp) {  // keys 32 kp .. 32 kp + 31
-              uint32_t m4[4];
-              ldsm_b8_trans_x2(m4, src + (2 * kp + pg) * (16 * D));
-              // m4[0]: keys 4(l%4) + 0..3 of d = l/4, m4[1]: of d + 8;
-              // m4[2], m4[3]: the same for the keys 16 later
-              uint32_t v[8];
+              for (int kp = 0; kp < 2; ++kp) {  // keys 32 kp .. 32 kp + 31
+                uint32_t m4[4];
+                ldsm_b8_trans_x2(m4, src + (2 * kp + pg) * (16 * D));
+                // m4[0]: keys 4(l%4) + 0..3 of d = l/4, m4[1]: of d + 8;
+                // m4[2], m4[3]: the same for the keys 16 later
+                uint32_t v[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                v[2 * e] = cvt_e4m3x2(m4[e]);
-                v[2 * e + 1] = cvt_e4m3x2(m4[e] >> 16);
+                for (int e = 0; e < 4; ++e) {
+                  v[2 * e] = fp8x2_to_f16x2<E5>(m4[e]);
+                  v[2 * e + 1] = fp8x2_to_f16x2<E5>(m4[e] >> 16);
+                }
+                tc::tmem_st_16x256b_x2(tbase + ((uint32_t)(32 * dq + 16 * dc) << 16) + C::VCOL +
+                                           vs * C::VTC + mh * 32 + kp * 16,
+                                       v);
               }
-              tc::tmem_st_16x256b_x2(tbase + ((uint32_t)(32 * dq + 16 * dc) << 16) + C::VCOL +
-                                         vs * C::VTC + mh * 32 + kp * 16,
-                                     v);
             }
           }
         }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(bar(kVReady + vs));
+        tc::mbar_arrive(bar(kVEmpty + st));
       }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      tc::mbar_arrive(bar(kVReady + vs));
-      tc::mbar_arrive(bar(kVEmpty + st));
-    }
+    };
+    if (p.kv_e5m2)
+      decode_v(std::true_type{});
+    else
+      decode_v(std::false_type{});
   } else if (warp < kWKDec) {
     // =============================== softmax (thread = key, NC rows)
     const int q = warp & 3, cg = warp >> 2;

@@ -84,7 +84,7 @@ typedef struct {
   int32_t max_seq_len;      /* launch capacity in tokens; 0 ->
                                block_table columns * page size */
   int32_t num_sms;          /* SMs the plan targets; 0 -> current device */
-  int32_t flags;            /* 0, or VAE4_FLAG_WARP_MMA */
+  int32_t flags;            /* 0, or VAE4_FLAG_WARP_MMA / VAE4_FLAG_KV_E5M2 */
 } vae4_options;
 
 /* Option flag: run the split stage on the warp-level tensor-core path
@@ -92,6 +92,16 @@ typedef struct {
  * tcgen05 / TMEM / TMA kernel.  Same contract and precision; kept as the
  * measured legacy baseline. */
 #define VAE4_FLAG_WARP_MMA 0x1
+
+/* Option flag: the KV bytes are OCP FP8 E5M2 (sign, 5-bit exponent with
+ * bias 15, 2-bit mantissa; largest finite value 57344) instead of E4M3.
+ * The pages keep the E5M2 cache format available beside E4M3 (PR #560,
+ * Purpose; PR #524, Scope and non-duplication).  Every finite E5M2 value is
+ * an FP16 value, so the decode stays exact; scales, state and combine are
+ * unchanged.  The infinity and NaN codes are outside the contract.  Only the
+ * default tcgen05 path implements it: with VAE4_FLAG_WARP_MMA the call
+ * returns VAE4_ERR_UNSUPPORTED. */
+#define VAE4_FLAG_KV_E5M2 0x2
 
 /* Return codes. */
 enum vae4_error {
@@ -254,7 +264,9 @@ int verify_attn_e4m3_clear_status(const vae4_tensor *workspace, vae4_stream stre
  * writes the raw FP16 bit patterns to dev_out (device, 256 x uint16).
  * flags selects the kernel as in vae4_options.flags: 0 = the tcgen05 path
  * (hardware converter, dec(b) exactly), VAE4_FLAG_WARP_MMA = the mma.sync
- * path (integer bit move, dec(b) * 2^-8 exactly).  *scale_log2 (host
+ * path (integer bit move, dec(b) * 2^-8 exactly), VAE4_FLAG_KV_E5M2 = the
+ * tcgen05 path's E5M2 decode (byte move, dec(b) exactly, infinities and
+ * NaNs as in FP16).  *scale_log2 (host
  * pointer) receives the exponent e with FP16 = dec(b) * 2^e; the kernels
  * fold 2^-e into their FP32 scales.  The NaN codes 0x7F / 0xFF are outside
  * the contract (NaN on the first decoder, a finite pattern on the second).

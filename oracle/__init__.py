@@ -57,14 +57,20 @@ def _load():
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint32]
             lib.oracle_e4m3_table.restype = None
             lib.oracle_e4m3_table.argtypes = [ctypes.c_void_p]
+            lib.oracle_e5m2_value.restype = ctypes.c_double
+            lib.oracle_e5m2_value.argtypes = [ctypes.c_uint32]
+            lib.oracle_fp8_table.restype = None
+            lib.oracle_fp8_table.argtypes = [ctypes.c_void_p, ctypes.c_int]
+            args = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                    ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                    ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
+                    ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
             lib.oracle_verify_attn.restype = ctypes.c_int
-            lib.oracle_verify_attn.argtypes = [
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
-                ctypes.c_double, ctypes.c_int, ctypes.c_void_p,
-                ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_verify_attn.argtypes = args
+            lib.oracle_verify_attn_fmt.restype = ctypes.c_int
+            lib.oracle_verify_attn_fmt.argtypes = args + [ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -83,6 +89,21 @@ def e4m3_table() -> np.ndarray:
     return out
 
 
+KV_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def e5m2_value(byte: int) -> float:
+    """OCP FP8 E5M2 decode of one byte (inf / NaN at exponent 31)."""
+    return _load().oracle_e5m2_value(int(byte) & 0xFF)
+
+
+def fp8_table(kv_format: str = "e4m3") -> np.ndarray:
+    """All 256 decoded values of the format, float64."""
+    out = np.empty(256, dtype=np.float64)
+    _load().oracle_fp8_table(out.ctypes.data, KV_FORMATS[kv_format])
+    return out
+
+
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
@@ -97,11 +118,11 @@ _ERRORS = {-1: "bad arguments", -2: "block id out of range",
 
 def verify_attn(q, kv_pages, block_table, seq_len, q_len, kv_scales,
                 sm_scale: float | None = None, split_tokens: int = 0,
-                rows=None, threads: int = 0) -> np.ndarray:
+                rows=None, threads: int = 0, kv_format: str = "e4m3") -> np.ndarray:
     """Exact (FP64) verify attention.
 
     q           float16/float32/float64 [B][Qmax][Hq][D]
-    kv_pages    uint8 [n_pages][2][Hkv][page][D] (E4M3 bytes; K at index 0)
+    kv_pages    uint8 [n_pages][2][Hkv][page][D] (FP8 bytes; K at index 0)
     block_table int32 [B][max_pages]
     seq_len     int32 [B]  (L, including the q tail)
     q_len       int32 [B]
@@ -110,6 +131,7 @@ def verify_attn(q, kv_pages, block_table, seq_len, q_len, kv_scales,
     split_tokens 0 = direct mode, else split mode with partitions of T tokens
     rows        None (all rows; returns [B][Qmax][Hq][D]) or an int array of
                 (b, i, hq) triples (returns [n_rows][D])
+    kv_format   "e4m3" (default) or "e5m2": how the KV bytes decode
     """
     lib = _load()
     q64 = np.ascontiguousarray(np.asarray(q).astype(np.float64))
@@ -134,11 +156,11 @@ def verify_attn(q, kv_pages, block_table, seq_len, q_len, kv_scales,
         out = np.zeros((r.shape[0], D), dtype=np.float64)
         rows_ptr, n_rows = r.ctypes.data, r.shape[0]
         rows = r  # keep alive
-    rc = lib.oracle_verify_attn(
+    rc = lib.oracle_verify_attn_fmt(
         q64.ctypes.data, kv.ctypes.data, bt.ctypes.data, sl.ctypes.data,
         ql.ctypes.data, sc.ctypes.data, B, Qmax, Hq, Hkv, D, page,
         n_pages, bt.shape[1], float(sm_scale), int(split_tokens), rows_ptr,
-        n_rows, out.ctypes.data, int(threads))
+        n_rows, out.ctypes.data, int(threads), KV_FORMATS[kv_format])
     if rc != 0:
         raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
     return out

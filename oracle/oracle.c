@@ -10,8 +10,14 @@
  *    bias 7, 3 mantissa bits, no infinities, NaN only at S.1111.111).  The
  *    pages require an exact decode checked on every byte (1Cat-vLLM PR #566
  *    "[Kernel] Finalize the audited TP2 DFlash2 31/29 ms endpoint", Final
- *    audit and Test Result) but do not define the format; the reading taken is the OCP definition, whose largest finite value
- *    is the 448 in the per-head scale amax/448.
+ *    audit and Test Result) but do not define the format; the reading taken
+ *    is the OCP definition, whose largest finite value is the 448 in the
+ *    per-head scale amax/448.
+ *
+ *  - E5M2 decode (the other FP8 KV format the pages keep available: PR #560,
+ *    Purpose; PR #524, Scope and non-duplication), OCP FP8 E5M2 (1 sign bit,
+ *    5 exponent bits with bias 15, 2 mantissa bits, infinities at
+ *    S.11111.00, NaN at S.11111.xx otherwise), largest finite value 57344.
  *
  *  - Per-KV-head dequantisation x = dec(byte) * s_h, with separate scales for
  *    K and V (PR #560 "[Bugfix] Use FP32 state and E4M3 defaults for
@@ -27,9 +33,9 @@
  *
  *  - Two evaluation modes.  Direct: two passes (maximum, then exponentials
  *    and sums).  Split: the context [0, L) is cut into partitions of T
- *    tokens; each keeps its own maximum, sum and unnormalised P.V (the FP32
- *    "max/sum and unnormalized PV until the final combine" of PR #524, final
- *    status), and the partitions are combined in ascending order.  Both give
+ *    tokens; each keeps its own FP32-style state, maximum, sum and
+ *    unnormalised P.V, merged only at the end (PR #524, final status), and
+ *    the partitions are combined in ascending order.  Both give
  *    the same exact result; the split mode exists so tests can pin that
  *    re-association.
  *
@@ -60,6 +66,25 @@ double oracle_e4m3_value(uint32_t byte) {
 
 void oracle_e4m3_table(double *out256) {
   for (int b = 0; b < 256; ++b) out256[b] = oracle_e4m3_value((uint32_t)b);
+}
+
+double oracle_e5m2_value(uint32_t byte) {
+  const int s = (byte >> 7) & 1;
+  const int e = (byte >> 2) & 31;
+  const int m = byte & 3;
+  double mag;
+  if (e == 31) return m == 0 ? (s ? -INFINITY : INFINITY) : NAN;
+  if (e == 0)
+    mag = ldexp((double)m, -16);          /* subnormal: m/4 * 2^(1-15)  */
+  else
+    mag = ldexp(4.0 + (double)m, e - 17); /* (1 + m/4) * 2^(e-15)       */
+  return s ? -mag : mag;
+}
+
+/* kv_format 0 = E4M3, 1 = E5M2 */
+void oracle_fp8_table(double *out256, int kv_format) {
+  for (int b = 0; b < 256; ++b)
+    out256[b] = kv_format == 1 ? oracle_e5m2_value((uint32_t)b) : oracle_e4m3_value((uint32_t)b);
 }
 
 /* Error codes of the oracle (independent of the library's). */
@@ -172,7 +197,8 @@ static int one_row(const double *q, const uint8_t *kv, const int32_t *bt,
 /*
  * Attention for the requested rows.
  *   q            [B][Qmax][Hq][D]      fp64 (the fp16 queries, widened exactly)
- *   kv           [n_pages][2][Hkv][page][D] E4M3 bytes
+ *   kv           [n_pages][2][Hkv][page][D] FP8 bytes (E4M3, or E5M2 when
+ *                kv_format == 1)
  *   block_table  [B][max_pages]        physical page ids
  *   seq_len      [B]                   L, including the q tail
  *   q_len        [B]                   queries in the tail (<= Qmax)
@@ -183,20 +209,20 @@ static int one_row(const double *q, const uint8_t *kv, const int32_t *bt,
  *   n_threads    OpenMP threads (0 = runtime default)
  * Returns ORC_OK or the first error code met.
  */
-int oracle_verify_attn(const double *q, const uint8_t *kv, const int32_t *block_table,
-                       const int32_t *seq_len, const int32_t *q_len,
-                       const double *scales, int B, int Qmax, int Hq, int Hkv,
-                       int D, int page, int64_t n_pages, int max_pages,
-                       double sm_scale, int split_tokens, const int32_t *rows,
-                       int64_t n_rows, double *out, int n_threads) {
+int oracle_verify_attn_fmt(const double *q, const uint8_t *kv, const int32_t *block_table,
+                           const int32_t *seq_len, const int32_t *q_len,
+                           const double *scales, int B, int Qmax, int Hq, int Hkv,
+                           int D, int page, int64_t n_pages, int max_pages,
+                           double sm_scale, int split_tokens, const int32_t *rows,
+                           int64_t n_rows, double *out, int n_threads, int kv_format) {
   if (B < 0 || Qmax <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || page <= 0 ||
-      max_pages <= 0 || Hq % Hkv != 0)
+      max_pages <= 0 || Hq % Hkv != 0 || kv_format < 0 || kv_format > 1)
     return ORC_BAD_ARGS;
   for (int b = 0; b < B; ++b)
     if (q_len[b] < 0 || q_len[b] > Qmax || seq_len[b] < 0) return ORC_BAD_ARGS;
   orc_shape sh = {B, Qmax, Hq, Hkv, D, page, max_pages, n_pages};
   double dec[256];
-  oracle_e4m3_table(dec);
+  oracle_fp8_table(dec, kv_format);
   int Lmax = 1;
   for (int b = 0; b < B; ++b) Lmax = seq_len[b] > Lmax ? seq_len[b] : Lmax;
   const int64_t total = rows ? n_rows : (int64_t)B * Qmax * Hq;
@@ -249,4 +275,16 @@ int oracle_max_threads(void) {
 #else
   return 1;
 #endif
+}
+
+/* The E4M3 entry point (kv_format 0). */
+int oracle_verify_attn(const double *q, const uint8_t *kv, const int32_t *block_table,
+                       const int32_t *seq_len, const int32_t *q_len,
+                       const double *scales, int B, int Qmax, int Hq, int Hkv,
+                       int D, int page, int64_t n_pages, int max_pages,
+                       double sm_scale, int split_tokens, const int32_t *rows,
+                       int64_t n_rows, double *out, int n_threads) {
+  return oracle_verify_attn_fmt(q, kv, block_table, seq_len, q_len, scales, B, Qmax, Hq, Hkv,
+                                D, page, n_pages, max_pages, sm_scale, split_tokens, rows,
+                                n_rows, out, n_threads, 0);
 }

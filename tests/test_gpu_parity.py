@@ -62,10 +62,12 @@ def oracle_full(w, seq_len=None, q_len=None):
     ql = w.q_len if q_len is None else q_len
     q = np.where(np.isnan(w.q), 0, w.q)  # padded slots are never read
     return oracle.verify_attn(q, w.kv_pages, w.block_table, sl, ql, w.kv_scales,
-                              sm_scale=w.sm_scale)
+                              sm_scale=w.sm_scale, kv_format=w.spec.kv_format)
 
 
 def check_full(w, **kw):
+    if w.spec.kv_format == "e5m2":
+        kw["flags"] = kw.get("flags", 0) | vae4.FLAG_KV_E5M2
     gpu, ws = run_gpu(w, **kw)
     ref = oracle_full(w)
     rel, mx = compare(gpu, ref)
@@ -282,3 +284,40 @@ def test_argument_errors_launch_nothing():
     with pytest.raises(vae4.Vae4Error) as e:   # a half-offset Q view
         vae4.verify(qv, kv, bt, seq, sc, out, ws, partition_tokens=256)
     assert e.value.code == -5
+
+
+# E5M2 KV cache (the second FP8 format), default tcgen05 path only
+E5M2 = [
+    dict(B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[3297, 1025], q_lens=[8, 5], seed=61,
+         partition_tokens=512, kv_format="e5m2"),
+    dict(B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[5000, 900], q_lens=[8, 8], seed=62,
+         outliers=True, kv_format="e5m2"),
+    dict(B=2, Qmax=8, Hq=8, Hkv=2, D=128, seq_lens=[1500, 999], q_lens=[8, 3], seed=63,
+         partition_tokens=256, kv_format="e5m2"),
+    dict(B=1, Qmax=16, Hq=4, Hkv=1, D=64, seq_lens=[2000], q_lens=[16], seed=64, page=1728,
+         kv_format="e5m2"),
+]
+
+
+@pytest.mark.parametrize("cfg", E5M2, ids=lambda c: str(c["seed"]))
+def test_parity_e5m2(cfg):
+    check_full(W.custom("e5m2", **cfg))
+
+
+def test_e5m2_decode_table_is_exact():
+    bits, e = vae4.decode_table(vae4.FLAG_KV_E5M2)
+    torch.cuda.synchronize()
+    assert e == 0
+    with np.errstate(invalid="ignore"):
+        h = bits.cpu().numpy().view(np.float16).astype(np.float64)
+    t = oracle.fp8_table("e5m2")
+    fin = np.isfinite(t)
+    assert np.array_equal(h[fin], t[fin])
+    assert np.array_equal(np.isinf(h), np.isinf(t)) and np.array_equal(np.isnan(h), np.isnan(t))
+    assert np.array_equal(np.signbit(h[np.isinf(t)]), np.signbit(t[np.isinf(t)]))
+
+
+def test_e5m2_with_warp_mma_path_is_unsupported():
+    w = W.custom("e5m2", **E5M2[0])
+    with pytest.raises(vae4.Vae4Error):
+        run_gpu(w, flags=vae4.FLAG_KV_E5M2 | vae4.FLAG_WARP_MMA)

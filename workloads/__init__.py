@@ -31,6 +31,7 @@ import math
 import numpy as np
 
 E4M3_MAX = np.float32(448.0)
+E5M2_MAX = np.float32(57344.0)
 PAGE = 16
 GEN_PAGES = 256      # 16-token pages per random-stream block (part of the recipe)
 
@@ -69,6 +70,42 @@ def quantize_e4m3(y: np.ndarray) -> np.ndarray:
     return code | (sign << 7)
 
 
+def quantize_e5m2(y: np.ndarray) -> np.ndarray:
+    """fp32 -> E5M2 bytes, round-to-nearest-even, saturating at +-57344.
+
+    Normal range (|y| >= 2^-14): round the fp32 significand to 2 bits the
+    same way as for E4M3 and re-bias the exponent (127 -> 15).  Subnormal
+    range: round |y| * 2^16 to an integer (half to even); 4 lands on the
+    smallest normal.
+    """
+    y = np.asarray(y, dtype=np.float32)
+    y = np.clip(y, -E5M2_MAX, E5M2_MAX)
+    sign = (y.view(np.uint32) >> 31).astype(np.uint8)
+    a = np.abs(y)
+    normal = a >= np.float32(2.0 ** -14)
+    u = a.view(np.uint32)
+    lsb = (u >> 21) & 1
+    ur = (u + np.uint32(0xFFFFF) + lsb) & np.uint32(0xFFE00000)
+    e5 = ((ur >> 23).astype(np.int32) - 127 + 15)
+    mant = ((ur >> 21) & 3).astype(np.int32)
+    code_n = (e5 << 2) | mant
+    code_s = np.rint(np.minimum(a, np.float32(2.0 ** -14)) * np.float32(65536.0)).astype(np.int32)
+    code = np.where(normal, code_n, code_s).astype(np.uint8)
+    return code | (sign << 7)
+
+
+def quantize(y: np.ndarray, kv_format: str = "e4m3") -> np.ndarray:
+    return quantize_e5m2(y) if kv_format == "e5m2" else quantize_e4m3(y)
+
+
+def fp8_scale(amax: np.float32, kv_format: str = "e4m3") -> np.float32:
+    """Per-head scale s = fp32(amax / largest finite value); zero amax -> 1."""
+    amax = np.float32(amax)
+    if amax == 0:
+        return np.float32(1.0)
+    return np.float32(amax / (E5M2_MAX if kv_format == "e5m2" else E4M3_MAX))
+
+
 def e4m3_scale(amax: np.float32) -> np.float32:
     """Per-head scale s = fp32(amax / 448); a zero amax gives s = 1."""
     amax = np.float32(amax)
@@ -98,6 +135,7 @@ class Spec:
     replays: list = dataclasses.field(default_factory=list)  # [(seq_lens, q_lens)]
     pad_q_nan: bool = False    # fill padded query slots with NaN
     q_from: tuple | None = None  # (spec name, row slice) to reuse queries
+    kv_format: str = "e4m3"    # stored FP8 format: "e4m3" or "e5m2"
 
 
 @dataclasses.dataclass
@@ -228,14 +266,14 @@ def generate(s: Spec | str) -> Workload:
                 amax = max(amax, np.float32(np.abs(x).max()))
                 if n_chunks <= 4:
                     cache.append(x)
-            sc = e4m3_scale(amax)
+            sc = fp8_scale(amax, s.kv_format)
             scales[h, sel] = sc
             for c in range(n_chunks):
                 n = min(chunk_pages, n_pages - c * chunk_pages)
                 x = cache[c] if cache else _kv_chunk(s.seed, sel, h, c, n, page, D,
                                                      s.outliers)
                 kv[c * chunk_pages:c * chunk_pages + n, sel, h] = \
-                    quantize_e4m3(x / sc)
+                    quantize(x / sc, s.kv_format)
 
     # queries
     if s.q_from is not None:
