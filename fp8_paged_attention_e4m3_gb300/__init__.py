@@ -18,6 +18,7 @@ VAE4_U8, VAE4_I32, VAE4_F16, VAE4_F32 = 1, 2, 3, 4
 
 FLAG_WARP_MMA = 0x1
 FLAG_KV_E5M2 = 0x2
+FLAG_BRIDGE_RAW = 0x4
 
 STATUS_BAD_BLOCK = 0x1
 STATUS_BAD_LENGTH = 0x2
@@ -39,6 +40,7 @@ EXPORTS = (
     "verify_attn_e4m3_strerror", "verify_attn_e4m3_read_status",
     "verify_attn_e4m3_clear_status", "verify_attn_e4m3_decode_table",
     "verify_attn_e4m3_noalloc", "verify_attn_e4m3_kv_read",
+    "verify_attn_e4m3_bridge_fp16",
 )
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -95,6 +97,9 @@ def load(build_if_stale: bool = True):
                      "verify_attn_e4m3_combine", "verify_attn_e4m3_kv_read"):
             getattr(lib, name).argtypes = [P] * 7 + [ctypes.c_void_p, ctypes.POINTER(Options)]
             getattr(lib, name).restype = ctypes.c_int
+        lib.verify_attn_e4m3_bridge_fp16.argtypes = [P] * 6 + [ctypes.c_void_p, ctypes.c_int32,
+                                                               ctypes.c_void_p]
+        lib.verify_attn_e4m3_bridge_fp16.restype = ctypes.c_int
         lib.verify_attn_e4m3_plan.argtypes = [ctypes.c_int] * 5 + [
             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
         lib.verify_attn_e4m3_plan.restype = ctypes.c_int
@@ -216,6 +221,21 @@ def verify_attn_e4m3_partials(*args, **kw):
 def verify_attn_e4m3_combine(*args, **kw):
     """Combine stage only (see the header)."""
     return _stage("verify_attn_e4m3_combine", *args, **kw)
+
+
+def verify_attn_e4m3_bridge_fp16(kv_pages, block_table, seq_lens, kv_scales, k_out, v_out,
+                                 *, status=None, flags: int = 0, stream=None):
+    """Paged FP8 -> dense FP16 K and V (see the header): k_out / v_out are
+    fp16 [B][Hkv][cap][D]; status is an optional int32 device tensor whose
+    first element receives the status bits."""
+    lib = load()
+    descs = [describe(t) for t in (kv_pages, block_table, seq_lens, kv_scales, k_out, v_out)]
+    st = ctypes.c_void_p(status.data_ptr()) if status is not None else ctypes.c_void_p(None)
+    rc = lib.verify_attn_e4m3_bridge_fp16(*[ctypes.byref(x) for x in descs], st,
+                                          ctypes.c_int32(int(flags)),
+                                          ctypes.c_void_p(_stream_handle(stream)))
+    _check(rc, "verify_attn_e4m3_bridge_fp16")
+    return k_out, v_out
 
 
 def verify_attn_e4m3_kv_read(*args, **kw):

@@ -277,9 +277,104 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   return VAE4_OK;
 }
 
+// Validation and parameters of the bridge call (kv, block table, lengths and
+// scales follow the verify step's rules; outputs are dense FP16 K and V).
+int prepare_bridge(const vae4_tensor *kv, const vae4_tensor *bt, const vae4_tensor *seq,
+                   const vae4_tensor *sc, const vae4_tensor *ko, const vae4_tensor *vo,
+                   uint32_t *status, int32_t flags, vae4::BridgeParams *bp, bool *empty) {
+  if (!kv || !bt || !seq || !sc || !ko || !vo) return VAE4_ERR_NULL;
+  if ((flags & ~(VAE4_FLAG_KV_E5M2 | VAE4_FLAG_BRIDGE_RAW)) != 0) return VAE4_ERR_OPTIONS;
+  if (kv->dtype != VAE4_U8 || bt->dtype != VAE4_I32 || seq->dtype != VAE4_I32 ||
+      sc->dtype != VAE4_F32 || ko->dtype != VAE4_F16 || vo->dtype != VAE4_F16)
+    return VAE4_ERR_DTYPE;
+  if (kv->ndim != 5 || kv->shape[1] != 2 || kv->shape[0] < 1 || kv->shape[2] < 1)
+    return VAE4_ERR_SHAPE;
+  const int64_t n_pages = kv->shape[0], Hkv = kv->shape[2], page = kv->shape[3], D = kv->shape[4];
+  if (D != 64 && D != 128 && D != 256) return VAE4_ERR_UNSUPPORTED;
+  if (page < 16 || page % 16 != 0 || page > 65536) return VAE4_ERR_UNSUPPORTED;
+  if (kv->stride[4] != 1 || kv->stride[3] != D || kv->stride[2] != page * D ||
+      kv->stride[1] != Hkv * page * D || kv->stride[0] != 2 * Hkv * page * D)
+    return VAE4_ERR_STRIDE;
+  if (!al16(kv->data)) return VAE4_ERR_MISALIGNED;
+  // outputs: F16 [B][Hkv][cap][D], d contiguous, rows on 16-byte boundaries
+  for (const vae4_tensor *o : {ko, vo}) {
+    if (o->ndim != 4 || o->shape[1] != Hkv || o->shape[3] != D || o->shape[2] < 1)
+      return VAE4_ERR_SHAPE;
+    if (o->shape[0] != ko->shape[0] || o->shape[2] != ko->shape[2]) return VAE4_ERR_SHAPE;
+    if (o->stride[3] != 1) return VAE4_ERR_STRIDE;
+    for (int k = 0; k < 3; ++k)
+      if (o->stride[k] < 0 || o->stride[k] % 8 != 0) return VAE4_ERR_STRIDE;
+    if (o->stride[0] != ko->stride[0] || o->stride[1] != ko->stride[1] ||
+        o->stride[2] != ko->stride[2])
+      return VAE4_ERR_STRIDE;
+    if (!al16(o->data)) return VAE4_ERR_MISALIGNED;
+  }
+  const int64_t B = ko->shape[0], cap = ko->shape[2];
+  if (B > 65535 || cap > INT32_MAX / 2) return VAE4_ERR_SHAPE;
+  if (bt->ndim != 2 || bt->shape[0] != B || bt->shape[1] < 1) return VAE4_ERR_SHAPE;
+  if (bt->stride[1] != 1 || bt->stride[0] < 0) return VAE4_ERR_STRIDE;
+  if (bt->shape[1] * page < cap) return VAE4_ERR_SHAPE;  // the table must address cap tokens
+  if (seq->ndim == 1) {
+    if (seq->shape[0] != B) return VAE4_ERR_SHAPE;
+  } else if (seq->ndim == 2) {
+    if (seq->shape[0] != B || seq->shape[1] != 2) return VAE4_ERR_SHAPE;
+    if (seq->stride[1] != 1) return VAE4_ERR_STRIDE;
+  } else {
+    return VAE4_ERR_SHAPE;
+  }
+  if (seq->stride[0] < 0 || seq->stride[0] > INT32_MAX) return VAE4_ERR_STRIDE;
+  if (sc->ndim != 2 || sc->shape[0] != Hkv || sc->shape[1] != 2) return VAE4_ERR_SHAPE;
+  if (sc->stride[1] != 1 || sc->stride[0] < 0 || sc->stride[0] > INT32_MAX) return VAE4_ERR_STRIDE;
+  *empty = B == 0;
+  if (B > 0 && (!kv->data || !bt->data || !seq->data || !sc->data || !ko->data || !vo->data))
+    return VAE4_ERR_NULL;
+  vae4::BridgeParams &p = *bp;
+  memset(&p, 0, sizeof(p));
+  p.kv = static_cast<const uint8_t *>(kv->data);
+  p.n_pages = n_pages;
+  p.bt = static_cast<const int32_t *>(bt->data);
+  p.bt_sb = bt->stride[0];
+  p.seq = static_cast<const int32_t *>(seq->data);
+  p.seq_sb = (int32_t)seq->stride[0];
+  p.scales = static_cast<const float *>(sc->data);
+  p.scale_sh = (int32_t)sc->stride[0];
+  p.k_out = static_cast<uint16_t *>(ko->data);
+  p.v_out = static_cast<uint16_t *>(vo->data);
+  p.o_sb = ko->stride[0];
+  p.o_sh = ko->stride[1];
+  p.o_st = ko->stride[2];
+  p.status = status;
+  p.B = (int32_t)B;
+  p.Hkv = (int32_t)Hkv;
+  p.D = (int32_t)D;
+  p.page = (int32_t)page;
+  p.cap = (int32_t)cap;
+  return VAE4_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int verify_attn_e4m3_bridge_fp16(const vae4_tensor *kv_pages, const vae4_tensor *block_table,
+                                 const vae4_tensor *seq_lens, const vae4_tensor *kv_scales,
+                                 const vae4_tensor *k_out, const vae4_tensor *v_out,
+                                 uint32_t *dev_status, int32_t flags, vae4_stream stream) {
+  vae4::BridgeParams bp;
+  bool empty = false;
+  int rc = prepare_bridge(kv_pages, block_table, seq_lens, kv_scales, k_out, v_out, dev_status,
+                          flags, &bp, &empty);
+  if (rc) return rc;
+  if (empty) return VAE4_OK;
+  int sms = 0;
+  rc = device_sms(&sms);
+  if (rc) return rc;
+  if (vae4::launch_bridge(bp, sms, (flags & VAE4_FLAG_KV_E5M2) != 0,
+                          (flags & VAE4_FLAG_BRIDGE_RAW) != 0,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
 
 int verify_attn_e4m3_ex(const vae4_tensor *q, const vae4_tensor *kv_pages,
                         const vae4_tensor *block_table, const vae4_tensor *seq_lens,

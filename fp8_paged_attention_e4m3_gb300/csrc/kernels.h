@@ -24,6 +24,8 @@ void tc_row_groups(int rows, int *n_rg, int *n);
 // Combine kernel (programmatic dependent launch after the split kernel).
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 cudaError_t launch_kv_read(const SplitParams &p, int num_sms, cudaStream_t stream);
+cudaError_t launch_bridge(const BridgeParams &p, int num_sms, bool e5m2, bool raw,
+                          cudaStream_t stream);
 
 // Decode-table test hook.
 cudaError_t launch_decode_table(uint16_t *out, bool integer_path, bool e5m2,

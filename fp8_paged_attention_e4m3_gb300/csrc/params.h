@@ -46,4 +46,20 @@ struct CombineParams {
   int32_t rows_pad, T, P, capacity;
 };
 
+// The bridge kernel's parameters (paged FP8 -> dense FP16 K and V).
+struct BridgeParams {
+  const uint8_t *kv;    // u8 [n_pages][2][Hkv][page][D]
+  int64_t n_pages;
+  const int32_t *bt;    // i32 [B][max_pages]
+  int64_t bt_sb;
+  const int32_t *seq;   // i32 [B] or [B][2] (L first)
+  int32_t seq_sb;
+  const float *scales;  // f32 [Hkv][2]
+  int32_t scale_sh;
+  uint16_t *k_out, *v_out;       // fp16 bits [B][Hkv][cap][D]
+  int64_t o_sb, o_sh, o_st;      // strides in elements (d stride 1)
+  uint32_t *status;     // optional sticky status word (device), may be null
+  int32_t B, Hkv, D, page, cap;
+};
+
 }  // namespace vae4

@@ -103,6 +103,9 @@ typedef struct {
  * returns VAE4_ERR_UNSUPPORTED. */
 #define VAE4_FLAG_KV_E5M2 0x2
 
+/* Bridge flag: write dec(byte) without the per-head scale (exact). */
+#define VAE4_FLAG_BRIDGE_RAW 0x4
+
 /* Return codes. */
 enum vae4_error {
   VAE4_OK = 0,
@@ -194,6 +197,34 @@ int verify_attn_e4m3_combine(const vae4_tensor *q, const vae4_tensor *kv_pages,
                              const vae4_tensor *kv_scales, const vae4_tensor *out,
                              const vae4_tensor *workspace, vae4_stream stream,
                              const vae4_options *opt);
+
+/*
+ * verify_attn_e4m3_bridge_fp16 -- the explicit paged-FP8 -> FP16 bridge the
+ * pages describe next to the grouped attention (PR #524 "[Kernel][SM70] Add
+ * opt-in E4M3 grouped attention with FP32 partials", historical R6 purpose
+ * and scope): the cache's decode and page gather as a call of its own.
+ *
+ *  kv_pages, block_table, seq_lens, kv_scales: as for verify_attn_e4m3
+ *              (seq_lens I32 [B] or [B][2]; only L is used).
+ *  k_out, v_out F16 [B][Hkv][cap][D], stride[3] == 1, other strides
+ *              multiples of 8 elements (equal for both), 16-byte aligned;
+ *              block_table must address cap tokens (columns * page >= cap).
+ *  dev_status  optional device pointer to a status word (NULL = none):
+ *              VAE4_STATUS_BAD_BLOCK / BAD_LENGTH bits are OR-ed in.
+ *  flags       VAE4_FLAG_KV_E5M2 (bytes are E5M2), VAE4_FLAG_BRIDGE_RAW.
+ *
+ * For every sequence b with 0 <= L <= cap and KV head h, token t < L:
+ *   k_out[b][h][t][:] = fp16(dec(K byte) * s_K[h]), v_out likewise with s_V,
+ * each rounded once (to nearest even) from the exact product; with
+ * VAE4_FLAG_BRIDGE_RAW, fp16(dec(byte)) (exact, no scale).  Tokens t >= L
+ * are not written.  A page with an invalid id writes zeros for its tokens
+ * and sets BAD_BLOCK; L > cap skips the sequence and sets BAD_LENGTH.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+int verify_attn_e4m3_bridge_fp16(const vae4_tensor *kv_pages, const vae4_tensor *block_table,
+                                 const vae4_tensor *seq_lens, const vae4_tensor *kv_scales,
+                                 const vae4_tensor *k_out, const vae4_tensor *v_out,
+                                 uint32_t *dev_status, int32_t flags, vae4_stream stream);
 
 /*
  * Measurement helper (not a step of the method): reads every KV byte that

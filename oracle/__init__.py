@@ -71,6 +71,12 @@ def _load():
             lib.oracle_verify_attn.argtypes = args
             lib.oracle_verify_attn_fmt.restype = ctypes.c_int
             lib.oracle_verify_attn_fmt.argtypes = args + [ctypes.c_int]
+            lib.oracle_bridge_fp16.restype = ctypes.c_int
+            lib.oracle_bridge_fp16.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_void_p]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -164,6 +170,32 @@ def verify_attn(q, kv_pages, block_table, seq_len, q_len, kv_scales,
     if rc != 0:
         raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
     return out
+
+
+def bridge_fp16(kv_pages, block_table, seq_len, kv_scales, cap: int,
+                kv_format: str = "e4m3", raw: bool = False):
+    """Exact values of the paged FP8 -> FP16 bridge, float64 [B][Hkv][cap][D]
+    for K and V: dec(byte) * scale for tokens t < L (dec(byte) when raw), NaN
+    where nothing is written (t >= L).  Round with round_to_fp16 to get the
+    FP16 the bridge must produce."""
+    lib = _load()
+    kv = np.ascontiguousarray(kv_pages, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_len, dtype=np.int32)
+    sc = np.ascontiguousarray(np.asarray(kv_scales).astype(np.float64))
+    n_pages, two, Hkv, page, D = kv.shape
+    B = sl.shape[0]
+    if two != 2 or bt.ndim != 2 or bt.shape[0] != B or sc.shape != (Hkv, 2):
+        raise ValueError("inconsistent shapes")
+    k = np.full((B, Hkv, cap, D), np.nan)
+    v = np.full((B, Hkv, cap, D), np.nan)
+    rc = lib.oracle_bridge_fp16(kv.ctypes.data, bt.ctypes.data, sl.ctypes.data, sc.ctypes.data,
+                                B, Hkv, D, page, n_pages, bt.shape[1], int(cap),
+                                KV_FORMATS[kv_format], int(bool(raw)), k.ctypes.data,
+                                v.ctypes.data)
+    if rc != 0:
+        raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
+    return k, v
 
 
 def round_to_fp16(x: np.ndarray) -> np.ndarray:

@@ -288,3 +288,51 @@ int oracle_verify_attn(const double *q, const uint8_t *kv, const int32_t *block_
                                 D, page, n_pages, max_pages, sm_scale, split_tokens, rows,
                                 n_rows, out, n_threads, 0);
 }
+
+/*
+ * Paged FP8 -> FP16 bridge, exact values (before the one rounding to FP16,
+ * which the caller applies): for sequence b, KV head h, token t < L,
+ *   k[b][h][t][d] = dec(K byte) * s_K[h],  v likewise with s_V[h]
+ * (raw != 0: dec(byte) alone), computed in FP64 (exact: a 4-bit by 24-bit
+ * product).  Entries for t >= L are left as they are.  Output arrays are
+ * dense [B][Hkv][cap][D].  Returns ORC_BAD_BLOCK / ORC_BAD_LENGTH on
+ * malformed inputs (first error met; the rest is still written).
+ */
+int oracle_bridge_fp16(const uint8_t *kv, const int32_t *block_table, const int32_t *seq_len,
+                       const double *scales, int B, int Hkv, int D, int page, int64_t n_pages,
+                       int max_pages, int cap, int kv_format, int raw, double *out_k,
+                       double *out_v) {
+  if (B < 0 || Hkv <= 0 || D <= 0 || page <= 0 || max_pages <= 0 || cap <= 0 ||
+      kv_format < 0 || kv_format > 1)
+    return ORC_BAD_ARGS;
+  double dec[256];
+  oracle_fp8_table(dec, kv_format);
+  int status = ORC_OK;
+  for (int b = 0; b < B; ++b) {
+    const int L = seq_len[b];
+    if (L < 0 || L > cap || (L + page - 1) / page > max_pages) {
+      if (status == ORC_OK) status = ORC_BAD_LENGTH;
+      continue;
+    }
+    for (int h = 0; h < Hkv; ++h) {
+      for (int t = 0; t < L; ++t) {
+        const int32_t phys = block_table[(int64_t)b * max_pages + t / page];
+        double *ok = out_k + (((int64_t)b * Hkv + h) * cap + t) * D;
+        double *ov = out_v + (((int64_t)b * Hkv + h) * cap + t) * D;
+        if (phys < 0 || phys >= n_pages) {
+          if (status == ORC_OK) status = ORC_BAD_BLOCK;
+          for (int d = 0; d < D; ++d) ok[d] = ov[d] = 0.0;
+          continue;
+        }
+        const uint8_t *kr = kv + ((((int64_t)phys * 2 + 0) * Hkv + h) * page + t % page) * D;
+        const uint8_t *vr = kv + ((((int64_t)phys * 2 + 1) * Hkv + h) * page + t % page) * D;
+        const double sk = raw ? 1.0 : scales[h * 2 + 0], sv = raw ? 1.0 : scales[h * 2 + 1];
+        for (int d = 0; d < D; ++d) {
+          ok[d] = dec[kr[d]] * sk;
+          ov[d] = dec[vr[d]] * sv;
+        }
+      }
+    }
+  }
+  return status;
+}
