@@ -312,6 +312,20 @@ def main():
     for i in range(NPAIR):
         for tag in (("a", "b") if i % 2 == 0 else ("b", "a")):
             samp[tag].append(timed(g_a if tag == "a" else g_b) * 1e3 / KB)
+    # ---- the paged FP8 -> FP16 bridge on the same cache: reads the KV bytes
+    # once and writes them as dense FP16 (3 bytes moved per element)
+    ko = torch.empty((s.B, s.Hkv, w.capacity, s.D), dtype=torch.float16, device=dev)
+    vo = torch.empty_like(ko)
+    g_br = torch.cuda.CUDAGraph()
+    NB = max(3, min(20, args.steps))
+    with torch.cuda.graph(g_br, stream=stream):
+        for k in range(NB):
+            vae4.verify_attn_e4m3_bridge_fp16(kvs[k % R], bt, seq, sc, ko, vo)
+    with torch.cuda.stream(stream):
+        g_br.replay()
+    torch.cuda.synchronize()
+    bridge_us = timed(g_br) * 1e3 / NB
+    del ko, vo
     clocks = sampler.stop()
     split_mean_us = split_total_ms * 1e3 / args.steps
     step_med, step_p90 = float(np.median(samp["a"])), float(np.percentile(samp["a"], 90))
@@ -387,6 +401,12 @@ def main():
                 "step_us_median": step_med, "step_us_p90": step_p90,
                 "step_over_floor": step_med / floor_med,
                 "samples": f"{NPAIR} ABBA pairs of {KB}-launch graph replays after 20 warm-up pairs"},
+            "bridge_fp16": {
+                "kernel": "verify_attn_e4m3_bridge_fp16 (paged E4M3 -> dense FP16 K and V)",
+                "us": bridge_us, "bytes": 3 * kv_bytes,
+                "gbs": 3 * kv_bytes / (bridge_us * 1e-6) / 1e9,
+                "frac": 3 * kv_bytes / (bridge_us * 1e-6) / 1e9 / peak,
+                "timing": f"{NB} back-to-back launches in one CUDA graph"},
             "gpu_launches": gpu_launches,
             "clocks": clocks,
             "gpu": props.name,

@@ -259,43 +259,60 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     tc::named_bar(2, kSetup);
   }
 
-  int issued[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // producers: uses issued per ring slot
+  int n_issued = 0;        // producers: half-tiles issued
   bool mma_issued = false;    // this thread issued tcgen05.mma
 
   if (producer) {
     // =============================== producers (K ring, V ring)
+    // Per half-tile, lanes 0-3 each issue one 16-key box (one page slice)
+    // in the same instruction.  Each lane keeps the (page, box-in-page) of
+    // its box and advances it by 4 boxes per half-tile: no division in the
+    // loop, whose length paces the whole stream.
     const bool isv = warp == kWVProd;
     const int nslot = isv ? C::NVR : C::NKR;
     const int fullb = isv ? kVFull : kKFull, emptyb = isv ? kVEmpty : kKEmpty;
     const uint32_t ring = isv ? sVR : sKR;
     if (lane == 0) tc::prefetch_tensormap(&tmap);
+    const int ppb = p.page >> 4;        // 16-key boxes per page
+    const int box0 = (k0 >> 4) + lane;  // lane g < 4: box g of the first half-tile
+    int lpg = box0 / ppb, sbg = box0 - lpg * ppb;
+    const int rowhead = (isv ? p.Hkv : 0) + h;  // row = (phys * 2Hkv + rowhead) * page + 16 sb
     for (int t = 0; t < nhalf; ++t) {
       const int st = t % nslot, u = t / nslot;
       if (t >= nslot && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
       if (lane == 0) tc::mbar_arrive_expect_tx(bar(fullb + st), C::RSLOT);
-      issued[st] = u + 1;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int key0 = k0 + 64 * t + 16 * g;
-        const int lp = key0 / p.page;  // a 16-key box never crosses a page
-        while (lp >= lp_base + 32) {  // advance the register window (warp-uniform)
-          cur = nxt;
-          lp_base += 32;
-          nxt = fetch(lp_base + 32 + lane);
+      n_issued = t + 1;
+      // block-table window: lane 0's page is in [lp_base, lp_base + 32) and
+      // the others' at most 3 pages on, so every box finds its id in cur/nxt
+      const int rel = lpg - lp_base;
+      const int pc = __shfl_sync(0xffffffffu, cur, rel & 31);
+      const int pn = __shfl_sync(0xffffffffu, nxt, rel & 31);
+      if (lane < 4) {
+        const int phys = rel < 32 ? pc : pn;
+        int row = (int)a.rows_total;  // outside the tensor: zero fill
+        if (k0 + 64 * t + 16 * lane < k1) {
+          if (phys >= 0 && phys < p.n_pages)
+            row = (phys * (2 * p.Hkv) + rowhead) * p.page + 16 * sbg;  // < 2^31 (checked)
+          else
+            *bad_f = 1;
         }
-        const int phys = __shfl_sync(0xffffffffu, cur, lp - lp_base);
-        if (lane == 0) {
-          int row = (int)a.rows_total;  // outside the tensor: zero fill
-          if (key0 < k1) {
-            if (phys >= 0 && phys < p.n_pages)
-              row = (int)(((int64_t)phys * 2 * p.Hkv + (isv ? p.Hkv : 0) + h) * p.page +
-                          (key0 - lp * p.page));
-            else
-              *bad_f = 1;
-          }
-          // one box: 16 keys x D bytes, as NDH blocks of 16 x IB (swizzled)
-          tc::tma_load_3d(ring + st * C::RSLOT + g * (16 * D), &tmap, 0, row, 0, bar(fullb + st));
+        // one box: 16 keys x D bytes, as NDH blocks of 16 x IB (swizzled)
+        tc::tma_load_3d(ring + st * C::RSLOT + lane * (16 * D), &tmap, 0, row, 0,
+                        bar(fullb + st));
+      }
+      if (ppb == 1) {
+        lpg += 4;
+      } else {
+        sbg += 4;
+        while (sbg >= ppb) {
+          sbg -= ppb;
+          ++lpg;
         }
+      }
+      if (__shfl_sync(0xffffffffu, lpg, 0) >= lp_base + 32) {  // slide the window
+        cur = nxt;
+        lp_base += 32;
+        nxt = fetch(lp_base + 32 + lane);
       }
     }
   } else if (warp == kWQk) {
@@ -661,8 +678,10 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     const int fullb = warp == kWVProd ? kVFull : kKFull;
     const int nslot = warp == kWVProd ? C::NVR : C::NKR;
     volatile int no_abort = 0;
-    for (int s = 0; s < nslot; ++s)
-      if (issued[s] > 0) tc::mbar_wait(bar(fullb + s), (issued[s] - 1) & 1, &no_abort, LIM);
+    for (int s = 0; s < nslot && s < n_issued; ++s) {
+      const int uses = (n_issued - 1 - s) / nslot + 1;  // half-tiles s, s + nslot, ...
+      tc::mbar_wait(bar(fullb + s), (uses - 1) & 1, &no_abort, LIM);
+    }
   }
   if (drain && (warp == kWQk || warp == kWPv) && lane == 0 && mma_issued) {
     const uint32_t db = bar(warp == kWQk ? kDrainQk : kDrainPv);
