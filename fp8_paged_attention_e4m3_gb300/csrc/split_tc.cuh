@@ -277,9 +277,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     const int box0 = (k0 >> 4) + lane;  // lane g < 4: box g of the first half-tile
     int lpg = box0 / ppb, sbg = box0 - lpg * ppb;
     const int rowhead = (isv ? p.Hkv : 0) + h;  // row = (phys * 2Hkv + rowhead) * page + 16 sb
+    int st = 0, u = 0;  // ring slot and pass of half-tile t (t = u * nslot + st)
     for (int t = 0; t < nhalf; ++t) {
-      const int st = t % nslot, u = t / nslot;
-      if (t >= nslot && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
+      if (u > 0 && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
       if (lane == 0) tc::mbar_arrive_expect_tx(bar(fullb + st), C::RSLOT);
       n_issued = t + 1;
       // block-table window: lane 0's page is in [lp_base, lp_base + 32) and
@@ -313,6 +313,10 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
         cur = nxt;
         lp_base += 32;
         nxt = fetch(lp_base + 32 + lane);
+      }
+      if (++st == nslot) {
+        st = 0;
+        ++u;
       }
     }
   } else if (warp == kWQk) {
