@@ -43,9 +43,20 @@ cudaError_t launch(const SplitParams &p, const TcArgs &a, const CUtensorMap &map
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  split_tc_kernel<D, N><<<dim3(p.P, p.Hkv * a.n_rg, p.B), C::NTHREADS, C::SMEM, stream>>>(p, a,
-                                                                                          map);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may be placed while the previous
+  // kernel on the stream drains; the kernel waits for it before its first
+  // global-memory access
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.P, p.Hkv * a.n_rg, p.B);
+  cfg.blockDim = dim3(C::NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<D, N>, p, a, map);
 }
 
 template <int D>

@@ -170,6 +170,11 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   const int row0 = rg * N;  // first row of this CTA's row group
   const bool producer = warp == kWKProd || warp == kWVProd;
 
+  // launched as a programmatic dependent: everything below may read what the
+  // previous kernel on the stream wrote (inputs) or overwrite what it reads
+  // (the workspace), so wait for it to finish first
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
   // producers: first block-table window, requested before anything else so
   // its latency overlaps the set-up.  Lane l holds logical page lp_base + l
   // (cur) and lp_base + 32 + l (nxt); entries past the row are -1, entries
