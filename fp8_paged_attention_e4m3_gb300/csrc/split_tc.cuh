@@ -278,6 +278,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     const int fullb = isv ? kVFull : kKFull, emptyb = isv ? kVEmpty : kKEmpty;
     const uint32_t ring = isv ? sVR : sKR;
     if (lane == 0) tc::prefetch_tensormap(&tmap);
+    // the KV stream is read once: keep it from pushing other data (the
+    // partials the combine reads, the block table) out of L2
+    const uint64_t pol = tc::l2_evict_first_policy();
     const int ppb = p.page >> 4;        // 16-key boxes per page
     const int box0 = (k0 >> 4) + lane;  // lane g < 4: box g of the first half-tile
     int lpg = box0 / ppb, sbg = box0 - lpg * ppb;
@@ -302,8 +305,8 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
             *bad_f = 1;
         }
         // one box: 16 keys x D bytes, as NDH blocks of 16 x IB (swizzled)
-        tc::tma_load_3d(ring + st * C::RSLOT + lane * (16 * D), &tmap, 0, row, 0,
-                        bar(fullb + st));
+        tc::tma_load_3d_hint(ring + st * C::RSLOT + lane * (16 * D), &tmap, 0, row, 0,
+                             bar(fullb + st), pol);
       }
       if (ppb == 1) {
         lpg += 4;
