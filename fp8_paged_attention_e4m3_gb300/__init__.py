@@ -19,6 +19,7 @@ VAE4_U8, VAE4_I32, VAE4_F16, VAE4_F32 = 1, 2, 3, 4
 FLAG_WARP_MMA = 0x1
 FLAG_KV_E5M2 = 0x2
 FLAG_BRIDGE_RAW = 0x4
+FLAG_TEST_SHORT_WAITS = 0x8
 
 STATUS_BAD_BLOCK = 0x1
 STATUS_BAD_LENGTH = 0x2

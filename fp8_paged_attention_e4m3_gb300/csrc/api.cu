@@ -102,15 +102,19 @@ struct Prepared {
   bool empty;
   bool warp_mma;
   int num_sms;
+  long long wait_limit;
 };
 
 // SM cycles a pipeline wait of the tcgen05 kernel may take before the CTA
 // gives up (about a second at the GB300 clock).
 constexpr long long kWaitLimitCycles = 2000000000LL;
+// VAE4_FLAG_TEST_SHORT_WAITS: every pipeline wait gives up after this many
+// cycles, far less than a memory round trip, so the call takes the abort path
+constexpr long long kShortWaitCycles = 256;
 
 cudaError_t launch_split(const Prepared &pr, cudaStream_t st) {
   return pr.warp_mma ? vae4::launch_split_mma(pr.sp, st)
-                     : vae4::launch_split_tc(pr.sp, kWaitLimitCycles, st);
+                     : vae4::launch_split_tc(pr.sp, pr.wait_limit, st);
 }
 
 int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
@@ -120,8 +124,9 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   vae4_options o;
   memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
-  if ((o.flags & ~(VAE4_FLAG_WARP_MMA | VAE4_FLAG_KV_E5M2)) != 0) return VAE4_ERR_OPTIONS;
-  if ((o.flags & VAE4_FLAG_WARP_MMA) && (o.flags & VAE4_FLAG_KV_E5M2))
+  if ((o.flags & ~(VAE4_FLAG_WARP_MMA | VAE4_FLAG_KV_E5M2 | VAE4_FLAG_TEST_SHORT_WAITS)) != 0)
+    return VAE4_ERR_OPTIONS;
+  if ((o.flags & VAE4_FLAG_WARP_MMA) && (o.flags & (VAE4_FLAG_KV_E5M2 | VAE4_FLAG_TEST_SHORT_WAITS)))
     return VAE4_ERR_UNSUPPORTED;
 
   int rc = check_qo(q);
@@ -203,6 +208,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   pr->ws_needed = lay.total;
   pr->empty = (B == 0);
   pr->warp_mma = (o.flags & VAE4_FLAG_WARP_MMA) != 0;
+  pr->wait_limit = (o.flags & VAE4_FLAG_TEST_SHORT_WAITS) ? kShortWaitCycles : kWaitLimitCycles;
   pr->num_sms = sms;
   if (B > 0 && ws->shape[0] < lay.total) return VAE4_ERR_WORKSPACE;
   if (!q->data || !kv->data || !bt->data || !seq->data || !sc->data || !out->data ||

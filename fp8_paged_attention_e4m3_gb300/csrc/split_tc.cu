@@ -90,6 +90,7 @@ cudaError_t launch_split_tc(const SplitParams &p, long long wait_limit, cudaStre
   TcArgs a;
   a.rows_total = p.n_pages * 2 * (int64_t)p.Hkv * p.page;
   a.wait_limit = wait_limit;
+  a.drain_limit = 2000000000LL;  // about a second: copies and MMAs always finish
   a.n_rg = n_rg;
   if (a.rows_total > (int64_t)0x7fffff00) return cudaErrorInvalidValue;
   // the pool as a 3-D tensor: (byte within an IB-wide block, row of D bytes,

@@ -65,7 +65,8 @@ namespace vae4 {
 
 struct TcArgs {
   int64_t rows_total;    // rows of D bytes in the pool view of the tensor map
-  long long wait_limit;  // SM cycles before a wait gives up
+  long long wait_limit;   // SM cycles before a pipeline wait gives up
+  long long drain_limit;  // SM cycles the wind-down waits for copies and MMAs in flight
   int32_t n_rg;          // row groups per KV head
 };
 
@@ -698,14 +699,14 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     volatile int no_abort = 0;
     for (int s = 0; s < nslot && s < n_issued; ++s) {
       const int uses = (n_issued - 1 - s) / nslot + 1;  // half-tiles s, s + nslot, ...
-      tc::mbar_wait(bar(fullb + s), (uses - 1) & 1, &no_abort, LIM);
+      tc::mbar_wait(bar(fullb + s), (uses - 1) & 1, &no_abort, a.drain_limit);
     }
   }
   if (drain && (warp == kWQk || warp == kWPv) && lane == 0 && mma_issued) {
     const uint32_t db = bar(warp == kWQk ? kDrainQk : kDrainPv);
     tc::mma_commit(db);
     volatile int no_abort = 0;
-    tc::mbar_wait(db, 0, &no_abort, LIM);
+    tc::mbar_wait(db, 0, &no_abort, a.drain_limit);
   }
   tc::tc_fence_before();
   __syncthreads();

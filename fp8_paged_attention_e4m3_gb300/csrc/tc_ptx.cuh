@@ -39,11 +39,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this many cycles select the failure-path test mode of
+// mbar_wait: give up unless the phase is already complete.
+constexpr long long kMinWaitLimit = 1024;
+
 // Bounded wait on the phase with the given parity.  Gives up (returns
 // false) when *abort is set by another thread or when `limit` SM cycles
 // pass; in the second case it sets *abort so every other role stops too.
+// (try_wait may suspend the thread until the phase completes, so the clock
+// is checked every 64 probes; a limit below kMinWaitLimit probes once,
+// without suspending.)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           long long limit) {
+  if (limit < kMinWaitLimit) {
+    if (mbar_test_wait(bar, parity)) return true;
+    *abort = 1;
+    return false;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {

@@ -103,6 +103,14 @@ typedef struct {
  * returns VAE4_ERR_UNSUPPORTED. */
 #define VAE4_FLAG_KV_E5M2 0x2
 
+/* Test hook for the failure path: every pipeline wait of the tcgen05 split
+ * kernel gives up after ~256 SM cycles instead of ~1 s, so the call aborts
+ * the way a stalled pipeline would (no fault: copies and MMAs in flight are
+ * still drained before the CTA exits), reports VAE4_STATUS_TIMEOUT and
+ * writes zero rows.  Not for production use; VAE4_ERR_UNSUPPORTED together
+ * with VAE4_FLAG_WARP_MMA. */
+#define VAE4_FLAG_TEST_SHORT_WAITS 0x8
+
 /* Bridge flag: write dec(byte) without the per-head scale (exact). */
 #define VAE4_FLAG_BRIDGE_RAW 0x4
 

@@ -321,3 +321,21 @@ def test_e5m2_with_warp_mma_path_is_unsupported():
     w = W.custom("e5m2", **E5M2[0])
     with pytest.raises(vae4.Vae4Error):
         run_gpu(w, flags=vae4.FLAG_KV_E5M2 | vae4.FLAG_WARP_MMA)
+
+
+def test_short_waits_report_timeout_and_the_context_recovers():
+    """Failure path without a GPU fault: with every pipeline wait cut to ~256
+    cycles the split kernel aborts (as a stalled pipeline would), drains its
+    copies and MMAs, reports VAE4_STATUS_TIMEOUT and the combine writes zero
+    rows.  The same workspace then serves a normal call that meets the bar."""
+    w = W.custom("abort", B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[3000, 1000], q_lens=[8, 8],
+                 seed=91)
+    tensors = W.to_device(w)
+    gpu, ws = run_gpu(w, tensors=tensors, flags=vae4.FLAG_TEST_SHORT_WAITS)
+    assert vae4.read_status(ws) & vae4.STATUS_TIMEOUT
+    assert np.isfinite(gpu).all() and not gpu.any()
+    vae4.clear_status(ws)
+    assert vae4.read_status(ws) == 0
+    gpu2, _ = run_gpu(w, tensors=tensors, ws=ws)
+    compare(gpu2, oracle_full(w))
+    assert vae4.read_status(ws) == 0
