@@ -25,6 +25,7 @@ STATUS_BAD_BLOCK = 0x1
 STATUS_BAD_LENGTH = 0x2
 STATUS_BAD_QLEN = 0x4
 STATUS_TIMEOUT = 0x8
+STATUS_PLAN = 0x10
 
 ERRORS = {
     0: "VAE4_OK", -1: "VAE4_ERR_NULL", -2: "VAE4_ERR_DTYPE", -3: "VAE4_ERR_SHAPE",

@@ -15,6 +15,7 @@
 namespace {
 
 using vae4::CombineParams;
+using vae4::kDevPlanMaxB;
 using vae4::SplitParams;
 
 constexpr int64_t kStatusBytes = 256;  // status word + padding
@@ -36,13 +37,44 @@ struct WsLayout {
   int64_t ml_off, o_off, total;
 };
 
-WsLayout ws_layout(int B, int Hkv, int P, int rows_pad, int D) {
+// status | (max, sum) [slots][rows][2] | unnormalised O [slots][rows][D]
+WsLayout ws_layout(int64_t slots, int rows_pad, int D) {
   WsLayout l;
   l.ml_off = kStatusBytes;
-  const int64_t ml_bytes = (int64_t)B * Hkv * P * rows_pad * 2 * 4;
+  const int64_t ml_bytes = slots * rows_pad * 2 * 4;
   l.o_off = align_up(l.ml_off + ml_bytes, 256);
-  l.total = l.o_off + (int64_t)B * Hkv * P * rows_pad * D * 4;
+  l.total = l.o_off + slots * rows_pad * D * 4;
   return l;
+}
+
+// Partial slots a launch needs: the static plan's B * Hkv * P, or with an
+// automatic plan the device plan's grid G = max(SMs, B * Hkv), whichever is
+// larger.
+int64_t ws_slots(int B, int Hkv, int P, int T_req, int sms) {
+  int64_t s = (int64_t)B * Hkv * P;
+  if (T_req == 0 && B > 1 && B <= kDevPlanMaxB) s = std::max<int64_t>(s, std::max<int64_t>(sms, (int64_t)B * Hkv));
+  return s;
+}
+
+// The device-side plan's partition length when every one of the B
+// sequences has L = cap (the same steps as the device code, with the counts
+// in closed form): the guess the split kernel prefetches block-table
+// entries for while it reads the actual lengths.
+int plan_width_equal(int B, int Hkv, int G, int cap) {
+  const int64_t gb = G / Hkv, sum = (int64_t)B * cap;
+  auto up16 = [](int64_t x) { return (int)((x + 15) & ~(int64_t)15); };
+  auto count = [&](int W) { return (int64_t)B * ((cap + W - 1) / W); };
+  int lo = std::max(64, up16((sum + gb - 1) / gb));
+  if (count(lo) <= gb) return lo;
+  int hi = gb > B ? std::max(lo, up16((sum + (gb - B) - 1) / (gb - B))) : std::max(64, up16(cap));
+  for (int it = 0; it < 6 && hi - lo > 16; ++it) {
+    const int mid = (int)(((int64_t)lo + hi) / 32 * 16);
+    if (count(mid) <= gb)
+      hi = mid;
+    else
+      lo = mid;
+  }
+  return hi;
 }
 
 int do_plan(int B, int Hkv, int cap, int T_req, int num_sms, int *T_out, int *P_out) {
@@ -204,7 +236,13 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
     rc = do_plan((int)B, (int)Hkv, (int)cap, o.partition_tokens, sms, &T, &P);
     if (rc) return rc;
   }
-  const WsLayout lay = ws_layout((int)B, (int)Hkv, P, (int)rows_pad, (int)D);
+  // automatic plans: one sequence takes its partition length from its L on
+  // the device (static grid); a batch gets the device-side balanced plan
+  const bool dev_plan = B > 1 && o.partition_tokens == 0 && B <= kDevPlanMaxB;
+  const bool t_from_len = o.partition_tokens == 0 && !dev_plan;
+  const int Gp = (int)std::max<int64_t>(sms, B * Hkv);  // device plan CTAs
+  const WsLayout lay =
+      ws_layout(ws_slots((int)B, (int)Hkv, P, o.partition_tokens, sms), (int)rows_pad, (int)D);
   pr->ws_needed = lay.total;
   pr->empty = (B == 0);
   pr->warp_mma = (o.flags & VAE4_FLAG_WARP_MMA) != 0;
@@ -256,6 +294,13 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   s.capacity = (int32_t)cap;
   s.sm_scale = sm_scale;
   s.kv_e5m2 = (o.flags & VAE4_FLAG_KV_E5M2) ? 1 : 0;
+  s.dev_plan = dev_plan ? 1 : 0;
+  s.t_from_len = t_from_len ? 1 : 0;
+  s.plan_G = Gp;
+  if (dev_plan) {
+    s.plan_W_guess = plan_width_equal((int)B, (int)Hkv, Gp, (int)cap);
+    s.plan_np_guess = (int)((cap + s.plan_W_guess - 1) / s.plan_W_guess);
+  }
 
   CombineParams &c = pr->cp;
   memset(&c, 0, sizeof(c));
@@ -278,8 +323,12 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   c.D = s.D;
   c.rows_pad = s.rows_pad;
   c.T = T;
-  c.P = P;
+  c.P = dev_plan ? std::max(P, Gp) : P;  // most partitions one stream can have
   c.capacity = s.capacity;
+  c.dev_plan = s.dev_plan;
+  c.t_from_len = s.t_from_len;
+  c.plan_G = Gp;
+  c.status = s.status;
   return VAE4_OK;
 }
 
@@ -476,7 +525,7 @@ int64_t verify_attn_e4m3_workspace_bytes(int B, int Hq, int Hkv, int Qmax, int D
   int T = 0, P = 0;
   const int rc = do_plan(B, Hkv, max_seq_len, partition_tokens, sms, &T, &P);
   if (rc) return rc;
-  return ws_layout(B, Hkv, P, (int)rows_pad, D).total;
+  return ws_layout(ws_slots(B, Hkv, P, partition_tokens, sms), (int)rows_pad, D).total;
 }
 
 int verify_attn_e4m3_abi_version(void) { return VAE4_ABI_VERSION; }

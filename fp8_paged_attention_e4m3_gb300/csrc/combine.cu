@@ -16,6 +16,8 @@
 // or pages were invalid get zeros.
 #include "common.cuh"
 #include "kernels.h"
+#include "plan.cuh"
+#include "verify_attn_e4m3.h"
 
 namespace vae4 {
 
@@ -37,6 +39,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   extern __shared__ __align__(16) float csm[];
   __shared__ float red[kCombineThreads / 32];
   __shared__ float4 accs[kGroups][kLanes];
+  __shared__ int plan_s[2];
 
   const int nd = p.D / 64;  // d slices per row
   const int r = blockIdx.x / nd, dsl = blockIdx.x - r * nd;
@@ -51,22 +54,48 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   // them before waiting for it
   const int L = p.seq[(int64_t)b * p.seq_sb];
   const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
+  // partitions of this (sequence, KV head): slots slot0 .. slot0 + nP - 1.
+  // The plan depends on the lengths alone, so it is evaluated before the wait.
+  int nP, slot0;
+  if (p.dev_plan) {
+    if (warp == 0) {  // lengths staged after the (m, l) and weight arrays
+      const PlanIn in{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G};
+      int *Ls = reinterpret_cast<int *>(csm + 2 * p.P);
+      plan_stage(in, Ls, lane);
+      const int2 sp = plan_stream_slots(in, Ls, b, h, lane);
+      if (lane == 0) {
+        if (sp.y < 0) atomicOr(p.status, VAE4_STATUS_PLAN);
+        plan_s[0] = sp.x;
+        plan_s[1] = sp.y;
+      }
+    }
+    __syncthreads();
+    slot0 = plan_s[0];
+    nP = plan_s[1];
+  } else {
+    slot0 = (b * p.Hkv + h) * p.P;
+    const int T = (p.t_from_len && L > 0 && L <= p.capacity) ? max(64, plan_t_from_len(L, p.P)) : p.T;
+    nP = (L + T - 1) / T;
+  }
+
   // wait until the split kernel's partials are complete and visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  const bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql;
-  const int nP = dead ? 0 : (L + p.T - 1) / p.T;
-
+  const bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql || nP < 0;
+  if (blockIdx.x == 0 && h == 0 && tid == 0) {  // report invalid lengths once per sequence
+    if (L < 0 || L > p.capacity) atomicOr(p.status, VAE4_STATUS_BAD_LENGTH);
+    else if (ql < 0 || ql > p.Qmax || (L > 0 && ql > L)) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
+  }
+  if (dead) nP = 0;
   float *wm = csm;       // m_p, then the weight w_p
   float *wl = csm + p.P; // l_p
   const int64_t pstride = (int64_t)p.rows_pad;  // rows per partition
-  const float *ml = p.ws_ml + (int64_t)(b * p.Hkv + h) * p.P * pstride * 2 + r * 2;
+  const float *ml = p.ws_ml + (int64_t)slot0 * pstride * 2 + r * 2;
   const float kNegInf = -__int_as_float(0x7f800000);
 
   // the first kPre P.V partials of this thread's group are requested now,
   // together with the (m, l) pairs, so both L2 round trips overlap
   const int l4 = tid % kLanes, grp = tid / kLanes;
-  const float *o = p.ws_o + (int64_t)(b * p.Hkv + h) * p.P * pstride * p.D + (int64_t)r * p.D +
-                   d0 + 4 * l4;
+  const float *o = p.ws_o + (int64_t)slot0 * pstride * p.D + (int64_t)r * p.D + d0 + 4 * l4;
   const int64_t ostride = pstride * p.D;
   constexpr int kPre = 10;  // covers 160 partitions
   float4 pre[kPre];
@@ -184,7 +213,8 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.Qmax * p.G * (p.D / 64), p.Hkv, p.B);
   cfg.blockDim = dim3(kCombineThreads);
-  cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float);
+  // (m_p, l_p) per partition; with the device plan, (L, q_len) per sequence
+  cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float) + (p.dev_plan ? (size_t)p.B * 2 * sizeof(int) : 0);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

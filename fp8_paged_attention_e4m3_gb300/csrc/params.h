@@ -5,6 +5,10 @@
 
 namespace vae4 {
 
+// The device-side balanced plan serves automatic plans of up to this many
+// sequences (every CTA scans the batch's lengths).
+constexpr int kDevPlanMaxB = 1024;
+
 // Everything a split (partition) kernel needs.  Strides are in elements.
 struct SplitParams {
   const void *q;        // fp16 [B][Qmax][Hq][D]
@@ -30,6 +34,10 @@ struct SplitParams {
   int32_t capacity;     // launch capacity (tokens)
   float sm_scale;       // softmax scale
   int32_t kv_e5m2;      // 1: the KV bytes are E5M2, 0: E4M3
+  int32_t dev_plan;     // 1: partitions from the device-side balanced plan (grid.x = G)
+  int32_t plan_G;       // device plan: CTAs along x = workspace slots
+  int32_t plan_W_guess, plan_np_guess;  // device plan when every L is the capacity
+  int32_t t_from_len;   // static grid: T = max(64, ceil16(L / P)) per sequence
 };
 
 // The combine kernel's parameters.
@@ -44,6 +52,9 @@ struct CombineParams {
   int32_t scale_sh;
   int32_t B, Qmax, Hq, Hkv, G, D;
   int32_t rows_pad, T, P, capacity;
+  int32_t dev_plan, plan_G;  // device-side balanced plan and its CTA count
+  int32_t t_from_len;        // static grid, T from each sequence's length
+  uint32_t *status;
 };
 
 // The bridge kernel's parameters (paged FP8 -> dense FP16 K and V).

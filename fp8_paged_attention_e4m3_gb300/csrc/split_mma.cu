@@ -15,6 +15,7 @@
 // token positions: moving pages changes no bit.
 #include "common.cuh"
 #include "kernels.h"
+#include "plan.cuh"
 #include "verify_attn_e4m3.h"
 
 namespace vae4 {
@@ -50,7 +51,26 @@ __global__ void __launch_bounds__(192, 1) split_mma_kernel(const SplitParams p) 
 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int part = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // static grid (partition, head, sequence) or the device-side balanced
+  // plan (grid.x = partition number), evaluated by every warp
+  int part, h, b, T;
+  int64_t pslot;
+  if (p.dev_plan) {
+    const PlanIn in{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G};
+    const int4 pl = plan_cta_global(in, blockIdx.x, lane);
+    if (pl.z < 0) return;  // past the plan
+    b = pl.x;
+    h = pl.y;
+    part = pl.z;
+    T = pl.w;
+    pslot = blockIdx.x;
+  } else {
+    part = blockIdx.x;
+    h = blockIdx.y;
+    b = blockIdx.z;
+    T = p.T;
+    pslot = (int64_t)(b * p.Hkv + h) * p.P + part;
+  }
 
   const int L = p.seq[(int64_t)b * p.seq_sb];
   const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
@@ -62,9 +82,10 @@ __global__ void __launch_bounds__(192, 1) split_mma_kernel(const SplitParams p) 
     if (part == 0 && h == 0 && tid == 0) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
     return;
   }
-  const int k0 = part * p.T;
+  if (!p.dev_plan && p.t_from_len && L > 0) T = max(64, plan_t_from_len(L, p.P));
+  const int k0 = part * T;
   if (k0 >= L) return;  // dead partition: never read by the combine
-  const int k1 = min(k0 + p.T, L);
+  const int k1 = min(k0 + T, L);
   const int ntiles = (k1 - k0 + kTK - 1) / kTK;
 
   // ---- queries: rows r = i*G + g of this KV head, padding rows zeroed
@@ -244,7 +265,7 @@ __global__ void __launch_bounds__(192, 1) split_mma_kernel(const SplitParams p) 
     l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, 2);
     l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 1);
     l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, 2);
-    const int64_t slot = ((int64_t)(b * p.Hkv + h) * p.P + part) * p.rows_pad;
+    const int64_t slot = pslot * p.rows_pad;
     if ((lane & 3) == 0) {
       p.ws_ml[(slot + r0) * 2 + 0] = m_run0;
       p.ws_ml[(slot + r0) * 2 + 1] = bad ? -1.f : l_run0;
@@ -274,7 +295,8 @@ int split_mma_threads(int rows_pad) {
 
 cudaError_t launch_split_mma(const SplitParams &p, cudaStream_t stream) {
   const size_t smem = split_mma_smem_bytes(p.D, p.rows_pad);
-  const dim3 grid(p.P, p.Hkv, p.B), block(split_mma_threads(p.rows_pad));
+  const dim3 grid = p.dev_plan ? dim3(p.plan_G, 1, 1) : dim3(p.P, p.Hkv, p.B);
+  const dim3 block(split_mma_threads(p.rows_pad));
   cudaError_t e = cudaSuccess;
   switch (p.D) {
     case 64:

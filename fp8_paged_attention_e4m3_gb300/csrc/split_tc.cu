@@ -4,7 +4,6 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -26,49 +25,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   });
   return fn;
-}
-
-template <int D, int N>
-cudaError_t launch(const SplitParams &p, const TcArgs &a, const CUtensorMap &map,
-                   cudaStream_t stream) {
-  using C = TcCfg<D, N>;
-  // the shared-memory opt-in is a per-device function attribute: set it once
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
-  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<D, N>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
-  }
-  // programmatic dependent launch: the CTAs may be placed while the previous
-  // kernel on the stream drains; the kernel waits for it before its first
-  // global-memory access
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.P, p.Hkv * a.n_rg, p.B);
-  cfg.blockDim = dim3(C::NTHREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<D, N>, p, a, map);
-}
-
-template <int D>
-cudaError_t launch_d(const SplitParams &p, const TcArgs &a, int n, const CUtensorMap &map,
-                     cudaStream_t stream) {
-  switch (n) {
-    case 16: return launch<D, 16>(p, a, map, stream);
-    case 32: return launch<D, 32>(p, a, map, stream);
-    case 48: return launch<D, 48>(p, a, map, stream);
-    case 64: return launch<D, 64>(p, a, map, stream);
-    default: return cudaErrorInvalidValue;
-  }
 }
 
 }  // namespace
@@ -107,12 +63,9 @@ cudaError_t launch_split_tc(const SplitParams &p, long long wait_limit, cudaStre
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  switch (D) {
-    case 64: return launch_d<64>(p, a, n, map, stream);
-    case 128: return launch_d<128>(p, a, n, map, stream);
-    case 256: return launch_d<256>(p, a, n, map, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  if (p.dev_plan) return launch_split_tc_dev(p, a, n, map, stream);
+  if (p.t_from_len) return launch_split_tc_len(p, a, n, map, stream);
+  return launch_tc_any<kPlanFixed>(p, a, n, map, stream);
 }
 
 }  // namespace vae4

@@ -53,11 +53,14 @@
 
 #include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
 #include "params.h"
+#include "plan.cuh"
 #include "tc_ptx.cuh"
 #include "verify_attn_e4m3.h"
 
@@ -126,6 +129,9 @@ enum : int {
   kWVDec = 12,     // 12..15
   kWKProd = 16, kWVProd = 17, kWQk = 18, kWPv = 19
 };
+// device-side plan scratch in the P^T buffer: (L, q_len) pairs of up to
+// kDevPlanMaxB sequences from byte 0, the published plan at byte kPlanSh
+constexpr int kPlanSh = 12288;
 // offsets in the small region (the mbarriers occupy its first 512 bytes)
 constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmVotes = 544, kSmM = 576,
               kSmPos = 832, kSmMNew = 1088, kSmBase = 1344, kSmThr = 1600,
@@ -133,7 +139,13 @@ constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmVotes = 544, kSmM
 
 __device__ __forceinline__ uint32_t sw128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
 
-template <int D, int N>
+// Partition plans, one instantiation each so none carries another's code:
+// kPlanFixed: static grid (partition, head x row group, sequence), T given;
+// kPlanFromLen: static grid, T from each sequence's length (the automatic
+// plan of one sequence); kPlanDevice: the device-side balanced plan
+// (grid.x = partition number, grid.y = row group).
+enum { kPlanFixed = 0, kPlanFromLen = 1, kPlanDevice = 2 };
+template <int D, int N, int MODE>
 __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     split_tc_kernel(const SplitParams p, const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
   using C = TcCfg<D, N>;
@@ -172,48 +184,11 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   float *red = reinterpret_cast<float *>(gSm + kSmRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int part = blockIdx.x, b = blockIdx.z;
-  const int h = blockIdx.y / a.n_rg, rg = blockIdx.y - h * a.n_rg;
-  const int row0 = rg * N;  // first row of this CTA's row group
   const bool producer = warp == kWKProd || warp == kWVProd;
 
-  // launched as a programmatic dependent: everything below may read what the
-  // previous kernel on the stream wrote (inputs) or overwrite what it reads
-  // (the workspace), so wait for it to finish first
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
-
-  // producers: first block-table window, requested before anything else so
-  // its latency overlaps the set-up.  Lane l holds logical page lp_base + l
-  // (cur) and lp_base + 32 + l (nxt); entries past the row are -1, entries
-  // past the sequence are loaded but never used.
-  const int32_t *btb = p.bt + (int64_t)b * p.bt_sb;
-  auto fetch = [&](int lp) -> int { return lp < p.max_pages ? __ldg(btb + lp) : -1; };
-  int lp_base = (part * p.T) / p.page;  // any page size that is a multiple of 16
-  int cur = -1, nxt = -1;
-  if (producer) {
-    cur = fetch(lp_base + lane);
-    nxt = fetch(lp_base + 32 + lane);
-  }
-
-  // ---- sequence, partition
-  const int L = p.seq[(int64_t)b * p.seq_sb];
-  const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
-  if (L < 0 || L > p.capacity) {
-    if (part == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, VAE4_STATUS_BAD_LENGTH);
-    return;
-  }
-  if (ql < 0 || ql > p.Qmax || (L > 0 && ql > L)) {
-    if (part == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
-    return;
-  }
-  const int k0 = part * p.T;
-  if (k0 >= L) return;  // dead partition
-  const int k1 = min(k0 + p.T, L);
-  const int ntiles = (k1 - k0 + 127) >> 7;
-  const int nhalf = 2 * ntiles;  // half-tiles, the last may be all padding
-
-  // ---- set-up: barriers and TMEM first (the producers start right after),
-  // then queries and per-row state (everyone else)
+  // ---- set-up that touches only this CTA's shared memory and TMEM, done
+  // before the grid dependency wait so it overlaps the previous kernel's
+  // tail: barriers, TMEM columns.
   if (tid == 0) {
     // arrival counts: TMA (expect_tx) and MMA commits arrive once; a K
     // half-tile is consumed by 2 decoder warps, a V half-tile by 4; K for a
@@ -232,6 +207,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     *abort_f = 0;
     *bad_f = 0;
   }
+  if (producer && lane == 0) tc::prefetch_tensormap(&tmap);  // a kernel parameter
   if (warp == kWQk) {
     tc::tmem_alloc(sSm + kSmTslot, 512);
     tc::tmem_relinquish();
@@ -241,10 +217,129 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t *>(gSm + kSmTslot);
+  // a CTA with nothing to do returns its TMEM columns before it exits (the
+  // conditions below are the same for all of its threads)
+  auto leave = [&]() {
+    if (warp == kWQk) tc::tmem_dealloc(tbase, 512);
+  };
+  // launched as a programmatic dependent: everything below may read what the
+  // previous kernel on the stream wrote (inputs) or overwrite what it reads
+  // (the workspace), so wait for it to finish first.  (Global reads before
+  // this point would also queue behind the previous kernel's stream.)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+  // ---- which partition: static grid (partition, head x row group,
+  // sequence) or the device-side plan (grid.x = partition number, grid.y =
+  // row group).
+  // producers: first block-table window, requested as early as possible.
+  // Lane l holds logical page lp_base + l (cur) and lp_base + 32 + l (nxt);
+  // entries past the row are -1, entries past the sequence are loaded but
+  // never used.
+  int part, b, h, T, L, ql;
+  int cur = -1, nxt = -1, lp_base = 0;
+  const int32_t *btb = p.bt;
+  auto fetch = [&](int lp) -> int { return lp < p.max_pages ? __ldg(btb + lp) : -1; };
+  auto fetch_bt = [&](int bb, int k0_) {
+    if (producer) {
+      btb = p.bt + (int64_t)bb * p.bt_sb;
+      lp_base = k0_ / p.page;  // any page size that is a multiple of 16
+      cur = fetch(lp_base + lane);
+      nxt = fetch(lp_base + 32 + lane);
+    }
+  };
+  if constexpr (MODE == kPlanDevice) {
+    // The plan needs the lengths first; meanwhile the producers fetch the
+    // block-table window of the plan for every sequence at the launch
+    // capacity (host-computed W and partitions per stream), which is the
+    // plan whenever the lengths are the capacity, and fetch again if not.
+    const int npg = p.plan_np_guess;
+    const int xs = (int)blockIdx.x / npg;  // stream of the guess
+    const int bg = xs / p.Hkv, k0g = ((int)blockIdx.x - xs * npg) * p.plan_W_guess;
+    if (bg < p.B) fetch_bt(bg, k0g);
+    // The K producer warp evaluates the plan and passes it on through the
+    // P^T buffer, unused until the first tile: the (L, q_len) pairs of the
+    // batch staged at its start, then b, h, p, W, L and q_len of sequence b
+    // at kPlanSh.
+    static_assert(C::PB >= kPlanSh + 64 && 2 * 4 * kDevPlanMaxB <= kPlanSh, "plan scratch");
+    int *plan_ls = reinterpret_cast<int *>(gP);
+    volatile int *plan_sh = reinterpret_cast<volatile int *>(gP + kPlanSh);
+    if (warp == kWKProd) {
+      const PlanIn pin{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G};
+      plan_stage(pin, plan_ls, lane);
+      const int4 pl = plan_cta(pin, plan_ls, blockIdx.x, lane);
+      if (lane == 0) {
+        plan_sh[0] = pl.x;
+        plan_sh[1] = pl.y;
+        plan_sh[2] = pl.z;
+        plan_sh[3] = pl.w;
+        plan_sh[4] = pl.z >= 0 ? plan_ls[2 * pl.x] : 0;
+        plan_sh[5] = pl.z >= 0 ? plan_ls[2 * pl.x + 1] : 0;
+      }
+    }
+    __syncthreads();
+    b = plan_sh[0];
+    h = plan_sh[1];
+    part = plan_sh[2];
+    T = plan_sh[3];
+    L = plan_sh[4];
+    ql = plan_sh[5];
+    if (part < 0)
+      b = h = part = L = ql = 0;  // past the plan: leaves below as a dead partition
+    else if (b != bg || part * T != k0g)
+      fetch_bt(b, part * T);  // not the guessed partition
+  } else {
+    part = blockIdx.x;
+    b = blockIdx.z;
+    h = blockIdx.y / a.n_rg;
+    T = p.T;
+    if constexpr (MODE != kPlanFromLen) fetch_bt(b, part * T);  // in flight with the length reads
+    L = p.seq[(int64_t)b * p.seq_sb];
+    ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
+    if constexpr (MODE == kPlanFromLen) {
+      // the sequence's P partitions share its L tokens; the block table is
+      // read once the length is known (fetching a guessed window first and
+      // fetching again when it misses cost more registers than it saved)
+      if (L > 0 && L <= p.capacity) T = max(64, plan_t_from_len(L, p.P));
+      fetch_bt(b, part * T);
+    }
+  }
+  // row group and workspace slot, from the CTA index alone (cheap to
+  // recompute where they are needed, in the epilogue)
+  constexpr bool DEV = MODE == kPlanDevice;
+  auto cta_rg = [&]() -> int { return DEV ? (int)blockIdx.y : (int)(blockIdx.y % a.n_rg); };
+  auto cta_slot = [&]() -> int64_t {
+    return DEV ? (int64_t)blockIdx.x
+               : ((int64_t)blockIdx.z * p.Hkv + blockIdx.y / a.n_rg) * p.P + blockIdx.x;
+  };
+  const int row0 = cta_rg() * N;  // first row of this CTA's row group
+
+  // ---- sequence, partition
+  if (L < 0 || L > p.capacity) {
+    if (part == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, VAE4_STATUS_BAD_LENGTH);
+    leave();
+    return;
+  }
+  if (ql < 0 || ql > p.Qmax || (L > 0 && ql > L)) {
+    if (part == 0 && blockIdx.y == 0 && tid == 0) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
+    leave();
+    return;
+  }
+  const int k0 = part * T;
+  // dead partition, or a row group whose rows are all past q_len (its
+  // queries are padding: the combine writes those rows as zeros)
+  if (k0 >= L || row0 >= ql * p.G) {
+    leave();
+    return;
+  }
+  const int k1 = min(k0 + T, L);
+  const int ntiles = (k1 - k0 + 127) >> 7;
+  const int nhalf = 2 * ntiles;  // half-tiles, the last may be all padding
+
   const long long LIM = a.wait_limit;
   // the combine kernel may be placed on SMs as they free up; it waits for
   // this grid's completion before reading any partial
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  // ---- queries and per-row state (everyone but the producers)
   constexpr int kSetup = C::NTHREADS - 64;  // every thread but the producers
   if (!producer) {
     const int st_id = tid < 32 * kWKProd ? tid : tid - 64;
@@ -284,7 +379,6 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     const int nslot = isv ? C::NVR : C::NKR;
     const int fullb = isv ? kVFull : kKFull, emptyb = isv ? kVEmpty : kKEmpty;
     const uint32_t ring = isv ? sVR : sKR;
-    if (lane == 0) tc::prefetch_tensormap(&tmap);
     // the KV stream is read once: keep it from pushing other data (the
     // partials the combine reads, the block table) out of L2
     const uint64_t pol = tc::l2_evict_first_policy();
@@ -658,7 +752,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
       const int q = warp & 3, k4 = warp >> 2;
       constexpr int NG = C::MH * (N / 8);        // 8-column groups per lane quadrant
       constexpr int GPW = (NG + 3) / 4;          // groups per warp
-      const int64_t slot = ((int64_t)(b * p.Hkv + h) * p.P + part) * p.rows_pad + row0;
+      const int64_t slot = cta_slot() * p.rows_pad + cta_rg() * N;
       uint32_t r[GPW][8];
 #pragma unroll
       for (int i = 0; i < GPW; ++i) {
@@ -722,10 +816,71 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     float l = 0.f;
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) l += red[(cg * 4 + qq) * 32 + c];
-    const int64_t slot = ((int64_t)(b * p.Hkv + h) * p.P + part) * p.rows_pad + row0;
+    const int64_t slot = cta_slot() * p.rows_pad + cta_rg() * N;
     p.ws_ml[(slot + r) * 2 + 0] = m_s[r];
     p.ws_ml[(slot + r) * 2 + 1] = (aborted || bad) ? -1.f : l;
   }
 }
+
+// ---------------------------------------------------------------------------
+// Host side: launch of one instantiation.
+template <int D, int N, int MODE>
+cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &map,
+                      cudaStream_t stream) {
+  using C = TcCfg<D, N>;
+  // the shared-memory opt-in is a per-device function attribute: set it once
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<D, N, MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  // programmatic dependent launch: the CTAs may be placed while the previous
+  // kernel on the stream drains; the kernel waits for it before its first
+  // global-memory access that depends on it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = MODE == kPlanDevice ? dim3(p.plan_G, a.n_rg, 1) : dim3(p.P, p.Hkv * a.n_rg, p.B);
+  cfg.blockDim = dim3(C::NTHREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<D, N, MODE>, p, a, map);
+}
+
+// Every (head dim, padded rows) instantiation of one plan mode.
+template <int MODE>
+cudaError_t launch_tc_any(const SplitParams &p, const TcArgs &a, int n, const CUtensorMap &map,
+                          cudaStream_t stream) {
+  switch (p.D * 1000 + n) {
+    case 64016: return launch_tc<64, 16, MODE>(p, a, map, stream);
+    case 64032: return launch_tc<64, 32, MODE>(p, a, map, stream);
+    case 64048: return launch_tc<64, 48, MODE>(p, a, map, stream);
+    case 64064: return launch_tc<64, 64, MODE>(p, a, map, stream);
+    case 128016: return launch_tc<128, 16, MODE>(p, a, map, stream);
+    case 128032: return launch_tc<128, 32, MODE>(p, a, map, stream);
+    case 128048: return launch_tc<128, 48, MODE>(p, a, map, stream);
+    case 128064: return launch_tc<128, 64, MODE>(p, a, map, stream);
+    case 256016: return launch_tc<256, 16, MODE>(p, a, map, stream);
+    case 256032: return launch_tc<256, 32, MODE>(p, a, map, stream);
+    case 256048: return launch_tc<256, 48, MODE>(p, a, map, stream);
+    case 256064: return launch_tc<256, 64, MODE>(p, a, map, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// The other plan modes' instantiations, each compiled in a translation unit
+// of its own.
+cudaError_t launch_split_tc_dev(const SplitParams &p, const TcArgs &a, int n,
+                                const CUtensorMap &map, cudaStream_t stream);
+cudaError_t launch_split_tc_len(const SplitParams &p, const TcArgs &a, int n,
+                                const CUtensorMap &map, cudaStream_t stream);
 
 }  // namespace vae4

@@ -1,0 +1,12 @@
+// The tcgen05 split kernel's device-side-plan instantiations, in a
+// translation unit of their own so the plan modes compile in parallel.
+#include "split_tc.cuh"
+
+namespace vae4 {
+
+cudaError_t launch_split_tc_dev(const SplitParams &p, const TcArgs &a, int n,
+                                const CUtensorMap &map, cudaStream_t stream) {
+  return launch_tc_any<kPlanDevice>(p, a, n, map, stream);
+}
+
+}  // namespace vae4

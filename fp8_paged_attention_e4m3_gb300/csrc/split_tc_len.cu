@@ -1,0 +1,14 @@
+// The tcgen05 split kernel's instantiations for a static grid whose
+// partition length follows each sequence's length (the automatic plan of a
+// single sequence), in a translation unit of their own so the plan modes
+// compile in parallel.
+#include "split_tc.cuh"
+
+namespace vae4 {
+
+cudaError_t launch_split_tc_len(const SplitParams &p, const TcArgs &a, int n,
+                                const CUtensorMap &map, cudaStream_t stream) {
+  return launch_tc_any<kPlanFromLen>(p, a, n, map, stream);
+}
+
+}  // namespace vae4

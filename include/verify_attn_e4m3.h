@@ -80,7 +80,9 @@ typedef struct {
 typedef struct {
   float softmax_scale;      /* 0 -> 1/sqrt(D) */
   int32_t partition_tokens; /* split-K partition length T (multiple of 16);
-                               0 -> automatic plan from the capacity */
+                               0 -> automatic plan, made on the device from
+                               the lengths of the call (see
+                               verify_attn_e4m3_plan) */
   int32_t max_seq_len;      /* launch capacity in tokens; 0 ->
                                block_table columns * page size */
   int32_t num_sms;          /* SMs the plan targets; 0 -> current device */
@@ -136,6 +138,8 @@ enum vae4_error {
 #define VAE4_STATUS_BAD_LENGTH 0x2u /* L < 0 or L > launch capacity */
 #define VAE4_STATUS_BAD_QLEN 0x4u   /* q_len < 0, q_len > Qmax, or q_len > L > 0 */
 #define VAE4_STATUS_TIMEOUT 0x8u    /* a bounded pipeline wait ran out */
+#define VAE4_STATUS_PLAN 0x10u      /* the device-side partition plan overran the grid
+                                       (an internal invariant; the rows are zeroed) */
 
 /*
  * verify_attn_e4m3 -- the verify step (split kernel + combine kernel).
@@ -264,6 +268,19 @@ int verify_attn_e4m3_kv_read(const vae4_tensor *q, const vae4_tensor *kv_pages,
  * pages' split used one partition per V100 SM: the 80 of the [80,8,6,2]
  * workspace, PR #524, final status).  num_sms must be > 0.
  * Returns VAE4_OK, VAE4_ERR_SHAPE or VAE4_ERR_PARTITION.
+ *
+ * That is the plan for sequences at the capacity.  A call with
+ * partition_tokens == 0 refines it on the device from the lengths it reads
+ * (so a captured graph stays balanced as the lengths change):
+ *  - B == 1 (or B > 1024): each sequence keeps the P partitions above and
+ *    takes T = max(64, ceil(L / P) rounded up to 16) from its own L;
+ *  - 1 < B <= 1024: the device-side balanced plan.  One length W, a
+ *    multiple of 16 and at least 64, for every (sequence, KV head) stream,
+ *    P_b = ceil(L_b / W), with sum_b Hkv * P_b <= G = max(num_sms, B*Hkv),
+ *    W from ceil(sum L / (G / Hkv)) and at most six bisection steps; the
+ *    partitions, numbered sequence-major, then KV head, then partition,
+ *    run as G CTAs (times the row groups) in one wave.
+ * Both give the same results as any fixed T up to FP32 rounding order.
  */
 int verify_attn_e4m3_plan(int B, int Hkv, int max_seq_len, int partition_tokens,
                           int num_sms, int32_t *partition_tokens_out,
@@ -274,7 +291,9 @@ int verify_attn_e4m3_plan(int B, int Hkv, int max_seq_len, int partition_tokens,
  * sizes needs: the status word, FP32 (max, sum) per partition and row
  * ([B][Hkv][P][rows][2], the pages' [80,8,6,2] "max/sum" layout, PR #524,
  * final status) and the FP32 unnormalised P.V per partition and row
- * ([B][Hkv][P][rows][D]); rows = Qmax * Hq/Hkv rounded up to 16.
+ * ([B][Hkv][P][rows][D]); rows = Qmax * Hq/Hkv rounded up to 16.  With
+ * partition_tokens == 0 and 1 < B <= 1024 the partials take
+ * max(B*Hkv*P, num_sms, B*Hkv) slots of [rows] (the device plan's grid).
  * num_sms == 0 queries the current device (a CUDA call); any other value
  * makes this a pure host computation.  Returns the size, or a negative
  * vae4_error.

@@ -78,12 +78,14 @@ def test_fullsize_sampled(name):
         assert d.max() <= 2e-3
 
 
-def test_rag_graph_replays():
+@pytest.mark.parametrize("T", [0, 2048], ids=["device-plan", "static-T2048"])
+def test_rag_graph_replays(T):
     """Ragged batch (log-uniform lengths 1K-256K incl. 1025 and 3297, q in
     {1, 8, 16}, NaN in padded query slots), one captured graph sized for
-    262144 tokens, lengths changed between replays, one replay with L = 0."""
+    262144 tokens, lengths changed between replays, one replay with L = 0.
+    T = 0: the device-side balanced plan, recomputed from the new lengths at
+    every replay; T = 2048: a static partition length."""
     w = workload("rag")
-    T = 2048  # ragged batches pass an explicit partition length
     q, kv, bt, seq, sc = W.to_device(w)
     out = torch.zeros_like(q)
     s = w.spec

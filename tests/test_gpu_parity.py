@@ -339,3 +339,60 @@ def test_short_waits_report_timeout_and_the_context_recovers():
     gpu2, _ = run_gpu(w, tensors=tensors, ws=ws)
     compare(gpu2, oracle_full(w))
     assert vae4.read_status(ws) == 0
+
+
+def test_device_plan_matches_static_plans_on_ragged_batches():
+    """The automatic (device-side balanced) plan and two static partition
+    lengths on the same ragged inputs: each meets the bar against the oracle."""
+    w = W.custom("ragged", B=5, Qmax=8, Hq=6, Hkv=1, D=256,
+                 seq_lens=[9000, 17, 3000, 0, 40000], q_lens=[8, 8, 1, 0, 8], seed=92)
+    ref = oracle_full(w)
+    live = np.zeros(ref.shape, bool)
+    for b in range(w.spec.B):
+        live[b, :int(w.q_len[b]) if w.seq_len[b] else 0] = True
+    for T in (0, 512, 4096):
+        gpu, ws = run_gpu(w, partition_tokens=T)
+        compare(gpu, ref, live)
+        assert not gpu[~live].any()
+        assert vae4.read_status(ws) == 0
+
+
+@pytest.mark.parametrize("B,Hkv,Hq,D", [(5, 1, 6, 256), (40, 2, 8, 128), (100, 1, 6, 64)])
+def test_device_plan_large_batches(B, Hkv, Hq, D):
+    """Up to 100 sequences, several KV heads, empty sequences and q_len = 0
+    among them (lengths far below the launch capacity, so no CTA's
+    block-table guess holds): the automatic plan meets the bar against the
+    oracle and leaves the status clear."""
+    rng = np.random.default_rng(B * 7 + Hkv)
+    seq = rng.integers(1, 1500, size=B)
+    ql = rng.integers(1, 9, size=B)
+    seq[::9] = 0
+    ql[::9] = 0
+    ql[min(5, B - 1)] = 0
+    ql = np.minimum(ql, seq)
+    w = W.custom("many", B=B, Qmax=8, Hq=Hq, Hkv=Hkv, D=D, seq_lens=seq.tolist(),
+                 q_lens=ql.tolist(), seed=93 + B)
+    ref = oracle_full(w)
+    live = np.zeros(ref.shape, bool)
+    for b in range(B):
+        live[b, :int(w.q_len[b]) if w.seq_len[b] else 0] = True
+    gpu, ws = run_gpu(w, partition_tokens=0)
+    compare(gpu, ref, live)
+    assert not gpu[~live].any()
+    assert vae4.read_status(ws) == 0
+
+
+@pytest.mark.parametrize("L", [1, 700, 5000, 12345, 20000])
+def test_single_sequence_auto_plan_below_capacity(L):
+    """One sequence in a launch sized for 20000 tokens: the automatic plan
+    spreads its L tokens over all of the launch's partitions; the result
+    meets the bar against the oracle at every length."""
+    w = W.custom("one", B=1, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[L], q_lens=[min(8, L)],
+                 capacity=20000, seed=94)
+    ref = oracle_full(w)
+    gpu, ws = run_gpu(w, partition_tokens=0)
+    live = np.zeros(ref.shape, bool)
+    live[0, :min(8, L)] = True
+    compare(gpu, ref, live)
+    assert not gpu[~live].any()
+    assert vae4.read_status(ws) == 0
