@@ -47,26 +47,41 @@ WsLayout ws_layout(int64_t slots, int rows_pad, int D) {
   return l;
 }
 
+// CTAs of the device-side plan: one wave on the SMs, at least one CTA per
+// (sequence, KV head, row group) so one partition per stream always fits.
+int vae4_tc_groups(int rows) {  // row groups of the tcgen05 kernel (the most any path uses)
+  int g = 1, n = 16;
+  vae4::tc_row_groups(rows, &g, &n);
+  return g;
+}
+
+int64_t dev_plan_ctas(int B, int Hkv, int n_rg, int sms) {
+  return std::max<int64_t>(sms, (int64_t)B * Hkv * n_rg);
+}
+
 // Partial slots a launch needs: the static plan's B * Hkv * P, or with an
-// automatic plan the device plan's grid G = max(SMs, B * Hkv), whichever is
-// larger.
-int64_t ws_slots(int B, int Hkv, int P, int T_req, int sms) {
+// automatic plan of a batch the device plan's grid, whichever is larger.
+int64_t ws_slots(int B, int Hkv, int P, int T_req, int sms, int n_rg) {
   int64_t s = (int64_t)B * Hkv * P;
-  if (T_req == 0 && B > 1 && B <= kDevPlanMaxB) s = std::max<int64_t>(s, std::max<int64_t>(sms, (int64_t)B * Hkv));
+  if (T_req == 0 && B > 1 && B <= kDevPlanMaxB && (int64_t)B * Hkv * n_rg <= 65535)
+    s = std::max<int64_t>(s, dev_plan_ctas(B, Hkv, n_rg, sms));
   return s;
 }
 
 // The device-side plan's partition length when every one of the B
-// sequences has L = cap (the same steps as the device code, with the counts
-// in closed form): the guess the split kernel prefetches block-table
-// entries for while it reads the actual lengths.
-int plan_width_equal(int B, int Hkv, int G, int cap) {
-  const int64_t gb = G / Hkv, sum = (int64_t)B * cap;
-  auto up16 = [](int64_t x) { return (int)((x + 15) & ~(int64_t)15); };
-  auto count = [&](int W) { return (int64_t)B * ((cap + W - 1) / W); };
+// sequences has L = cap and r row groups (the same steps as the device
+// code, with the counts in closed form): the guess the split kernel
+// prefetches block-table entries for while it reads the actual lengths.
+int plan_width_equal(int B, int Hkv, int G, int cap, int r) {
+  const int64_t gb = G / Hkv, nrg = (int64_t)B * r, sum = nrg * cap;
+  auto up16 = [](int64_t x) { return (int)std::min<int64_t>((x + 15) & ~(int64_t)15, 0x7FFFFFF0); };
+  auto count = [&](int W) { return nrg * ((cap + W - 1) / W); };
   int lo = std::max(64, up16((sum + gb - 1) / gb));
   if (count(lo) <= gb) return lo;
-  int hi = gb > B ? std::max(lo, up16((sum + (gb - B) - 1) / (gb - B))) : std::max(64, up16(cap));
+  int hi = std::max(64, up16(cap));
+  if (gb > nrg && sum / 65536 / (gb - nrg) < (1 << 14))
+    hi = std::min(hi, up16((sum + (gb - nrg) - 1) / (gb - nrg)));
+  hi = std::max(hi, lo);
   for (int it = 0; it < 6 && hi - lo > 16; ++it) {
     const int mid = (int)(((int64_t)lo + hi) / 32 * 16);
     if (count(mid) <= gb)
@@ -238,11 +253,16 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   }
   // automatic plans: one sequence takes its partition length from its L on
   // the device (static grid); a batch gets the device-side balanced plan
-  const bool dev_plan = B > 1 && o.partition_tokens == 0 && B <= kDevPlanMaxB;
+  const bool dev_plan = B > 1 && o.partition_tokens == 0 && B <= kDevPlanMaxB &&
+                        B * Hkv * vae4_tc_groups((int)rows) <= 65535;  // grid.y limit
   const bool t_from_len = o.partition_tokens == 0 && !dev_plan;
-  const int Gp = (int)std::max<int64_t>(sms, B * Hkv);  // device plan CTAs
-  const WsLayout lay =
-      ws_layout(ws_slots((int)B, (int)Hkv, P, o.partition_tokens, sms), (int)rows_pad, (int)D);
+  // rows per CTA: row groups of the tcgen05 kernel, all rows on the mma.sync path
+  int n_rg = 1, n_rows = (int)rows_pad;
+  if (!(o.flags & VAE4_FLAG_WARP_MMA)) vae4::tc_row_groups((int)rows, &n_rg, &n_rows);
+  const int Gp = (int)dev_plan_ctas((int)B, (int)Hkv, n_rg, sms);  // device plan CTAs
+  const WsLayout lay = ws_layout(ws_slots((int)B, (int)Hkv, P, o.partition_tokens, sms,
+                                          vae4_tc_groups((int)rows)),
+                                 (int)rows_pad, (int)D);
   pr->ws_needed = lay.total;
   pr->empty = (B == 0);
   pr->warp_mma = (o.flags & VAE4_FLAG_WARP_MMA) != 0;
@@ -297,8 +317,10 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   s.dev_plan = dev_plan ? 1 : 0;
   s.t_from_len = t_from_len ? 1 : 0;
   s.plan_G = Gp;
+  s.plan_N = n_rows;
   if (dev_plan) {
-    s.plan_W_guess = plan_width_equal((int)B, (int)Hkv, Gp, (int)cap);
+    const int rg_guess = (int)((Qmax * s.G + n_rows - 1) / n_rows);  // row groups at Qmax
+    s.plan_W_guess = plan_width_equal((int)B, (int)Hkv, Gp, (int)cap, rg_guess);
     s.plan_np_guess = (int)((cap + s.plan_W_guess - 1) / s.plan_W_guess);
   }
 
@@ -328,6 +350,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   c.dev_plan = s.dev_plan;
   c.t_from_len = s.t_from_len;
   c.plan_G = Gp;
+  c.plan_N = n_rows;
   c.status = s.status;
   return VAE4_OK;
 }
@@ -525,7 +548,9 @@ int64_t verify_attn_e4m3_workspace_bytes(int B, int Hq, int Hkv, int Qmax, int D
   int T = 0, P = 0;
   const int rc = do_plan(B, Hkv, max_seq_len, partition_tokens, sms, &T, &P);
   if (rc) return rc;
-  return ws_layout(ws_slots(B, Hkv, P, partition_tokens, sms), (int)rows_pad, D).total;
+  return ws_layout(ws_slots(B, Hkv, P, partition_tokens, sms, vae4_tc_groups(Qmax * (Hq / Hkv))),
+                   (int)rows_pad, D)
+      .total;
 }
 
 int verify_attn_e4m3_abi_version(void) { return VAE4_ABI_VERSION; }

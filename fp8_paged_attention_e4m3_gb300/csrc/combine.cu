@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   int nP, slot0;
   if (p.dev_plan) {
     if (warp == 0) {  // lengths staged after the (m, l) and weight arrays
-      const PlanIn in{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G};
+      const PlanIn in{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G,
+                      p.G, p.plan_N};
       int *Ls = reinterpret_cast<int *>(csm + 2 * p.P);
       plan_stage(in, Ls, lane);
       const int2 sp = plan_stream_slots(in, Ls, b, h, lane);

@@ -36,6 +36,7 @@ struct SplitParams {
   int32_t kv_e5m2;      // 1: the KV bytes are E5M2, 0: E4M3
   int32_t dev_plan;     // 1: partitions from the device-side balanced plan (grid.x = G)
   int32_t plan_G;       // device plan: CTAs along x = workspace slots
+  int32_t plan_N;       // device plan: rows per CTA (a row group)
   int32_t plan_W_guess, plan_np_guess;  // device plan when every L is the capacity
   int32_t t_from_len;   // static grid: T = max(64, ceil16(L / P)) per sequence
 };
@@ -53,6 +54,7 @@ struct CombineParams {
   int32_t B, Qmax, Hq, Hkv, G, D;
   int32_t rows_pad, T, P, capacity;
   int32_t dev_plan, plan_G;  // device-side balanced plan and its CTA count
+  int32_t plan_N;            // device plan: rows per split CTA
   int32_t t_from_len;        // static grid, T from each sequence's length
   uint32_t *status;
 };

@@ -56,13 +56,14 @@ __global__ void __launch_bounds__(192, 1) split_mma_kernel(const SplitParams p) 
   int part, h, b, T;
   int64_t pslot;
   if (p.dev_plan) {
-    const PlanIn in{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G};
-    const int4 pl = plan_cta_global(in, blockIdx.x, lane);
-    if (pl.z < 0) return;  // past the plan
-    b = pl.x;
-    h = pl.y;
-    part = pl.z;
-    T = pl.w;
+    const PlanIn in{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G,
+                    p.G, p.plan_N};
+    const PlanCta c = plan_cta_global(in, blockIdx.x, lane);
+    if (c.p < 0) return;  // past the plan
+    b = c.b;
+    h = c.h;
+    part = c.p;
+    T = c.W;
     pslot = blockIdx.x;
   } else {
     part = blockIdx.x;

@@ -357,20 +357,23 @@ def test_device_plan_matches_static_plans_on_ragged_batches():
         assert vae4.read_status(ws) == 0
 
 
-@pytest.mark.parametrize("B,Hkv,Hq,D", [(5, 1, 6, 256), (40, 2, 8, 128), (100, 1, 6, 64)])
-def test_device_plan_large_batches(B, Hkv, Hq, D):
+@pytest.mark.parametrize("B,Hkv,Hq,D,Qmax", [(5, 1, 6, 256, 8), (40, 2, 8, 128, 8),
+                                              (100, 1, 6, 64, 8), (12, 1, 6, 128, 16),
+                                              (7, 2, 12, 256, 16)])
+def test_device_plan_large_batches(B, Hkv, Hq, D, Qmax):
     """Up to 100 sequences, several KV heads, empty sequences and q_len = 0
-    among them (lengths far below the launch capacity, so no CTA's
+    among them, up to 16 queries (two row groups, the second busy only for
+    some sequences; lengths far below the launch capacity, so no CTA's
     block-table guess holds): the automatic plan meets the bar against the
     oracle and leaves the status clear."""
     rng = np.random.default_rng(B * 7 + Hkv)
     seq = rng.integers(1, 1500, size=B)
-    ql = rng.integers(1, 9, size=B)
+    ql = rng.integers(1, Qmax + 1, size=B)
     seq[::9] = 0
     ql[::9] = 0
     ql[min(5, B - 1)] = 0
     ql = np.minimum(ql, seq)
-    w = W.custom("many", B=B, Qmax=8, Hq=Hq, Hkv=Hkv, D=D, seq_lens=seq.tolist(),
+    w = W.custom("many", B=B, Qmax=Qmax, Hq=Hq, Hkv=Hkv, D=D, seq_lens=seq.tolist(),
                  q_lens=ql.tolist(), seed=93 + B)
     ref = oracle_full(w)
     live = np.zeros(ref.shape, bool)
