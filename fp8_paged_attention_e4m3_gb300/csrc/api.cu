@@ -34,16 +34,18 @@ int64_t ws_rows(int rows) {
 }
 
 struct WsLayout {
-  int64_t ml_off, o_off, total;
+  int64_t ml_off, o_off, tab_off, total;
 };
 
-// status | (max, sum) [slots][rows][2] | unnormalised O [slots][rows][D]
-WsLayout ws_layout(int64_t slots, int rows_pad, int D) {
+// status | (max, sum) [slots][rows][2] | unnormalised O [slots][rows][D] |
+// (first slot, partitions) [B][Hkv] of the device-side plan
+WsLayout ws_layout(int64_t slots, int rows_pad, int D, int64_t streams) {
   WsLayout l;
   l.ml_off = kStatusBytes;
   const int64_t ml_bytes = slots * rows_pad * 2 * 4;
   l.o_off = align_up(l.ml_off + ml_bytes, 256);
-  l.total = l.o_off + slots * rows_pad * D * 4;
+  l.tab_off = align_up(l.o_off + slots * rows_pad * D * 4, 256);
+  l.total = l.tab_off + streams * 8;  // device plan: (first slot, partitions) per stream
   return l;
 }
 
@@ -254,7 +256,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   // automatic plans: one sequence takes its partition length from its L on
   // the device (static grid); a batch gets the device-side balanced plan
   const bool dev_plan = B > 1 && o.partition_tokens == 0 && B <= kDevPlanMaxB &&
-                        B * Hkv * vae4_tc_groups((int)rows) <= 65535;  // grid.y limit
+                        B * Hkv * vae4_tc_groups((int)rows) <= 65535;
   const bool t_from_len = o.partition_tokens == 0 && !dev_plan;
   // rows per CTA: row groups of the tcgen05 kernel, all rows on the mma.sync path
   int n_rg = 1, n_rows = (int)rows_pad;
@@ -262,7 +264,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   const int Gp = (int)dev_plan_ctas((int)B, (int)Hkv, n_rg, sms);  // device plan CTAs
   const WsLayout lay = ws_layout(ws_slots((int)B, (int)Hkv, P, o.partition_tokens, sms,
                                           vae4_tc_groups((int)rows)),
-                                 (int)rows_pad, (int)D);
+                                 (int)rows_pad, (int)D, B * Hkv);
   pr->ws_needed = lay.total;
   pr->empty = (B == 0);
   pr->warp_mma = (o.flags & VAE4_FLAG_WARP_MMA) != 0;
@@ -299,6 +301,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   s.scale_sh = (int32_t)sc->stride[0];
   s.ws_ml = reinterpret_cast<float *>(wsb + lay.ml_off);
   s.ws_o = reinterpret_cast<float *>(wsb + lay.o_off);
+  s.plan_tab = reinterpret_cast<int2 *>(wsb + lay.tab_off);
   s.status = reinterpret_cast<uint32_t *>(wsb);
   s.B = (int32_t)B;
   s.Qmax = (int32_t)Qmax;
@@ -351,6 +354,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   c.t_from_len = s.t_from_len;
   c.plan_G = Gp;
   c.plan_N = n_rows;
+  c.plan_tab = s.plan_tab;
   c.status = s.status;
   return VAE4_OK;
 }
@@ -549,7 +553,7 @@ int64_t verify_attn_e4m3_workspace_bytes(int B, int Hq, int Hkv, int Qmax, int D
   const int rc = do_plan(B, Hkv, max_seq_len, partition_tokens, sms, &T, &P);
   if (rc) return rc;
   return ws_layout(ws_slots(B, Hkv, P, partition_tokens, sms, vae4_tc_groups(Qmax * (Hq / Hkv))),
-                   (int)rows_pad, D)
+                   (int)rows_pad, D, (int64_t)B * Hkv)
       .total;
 }
 

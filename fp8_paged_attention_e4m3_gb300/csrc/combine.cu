@@ -39,7 +39,6 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   extern __shared__ __align__(16) float csm[];
   __shared__ float red[kCombineThreads / 32];
   __shared__ float4 accs[kGroups][kLanes];
-  __shared__ int plan_s[2];
 
   const int nd = p.D / 64;  // d slices per row
   const int r = blockIdx.x / nd, dsl = blockIdx.x - r * nd;
@@ -54,26 +53,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   // them before waiting for it
   const int L = p.seq[(int64_t)b * p.seq_sb];
   const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
-  // partitions of this (sequence, KV head): slots slot0 .. slot0 + nP - 1.
-  // The plan depends on the lengths alone, so it is evaluated before the wait.
-  int nP, slot0;
-  if (p.dev_plan) {
-    if (warp == 0) {  // lengths staged after the (m, l) and weight arrays
-      const PlanIn in{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv, p.plan_G,
-                      p.G, p.plan_N};
-      int *Ls = reinterpret_cast<int *>(csm + 2 * p.P);
-      plan_stage(in, Ls, lane);
-      const int2 sp = plan_stream_slots(in, Ls, b, h, lane);
-      if (lane == 0) {
-        if (sp.y < 0) atomicOr(p.status, VAE4_STATUS_PLAN);
-        plan_s[0] = sp.x;
-        plan_s[1] = sp.y;
-      }
-    }
-    __syncthreads();
-    slot0 = plan_s[0];
-    nP = plan_s[1];
-  } else {
+  // partitions of this (sequence, KV head): slots slot0 .. slot0 + nP - 1
+  int nP = 0, slot0 = 0;
+  if (!p.dev_plan) {
     slot0 = (b * p.Hkv + h) * p.P;
     const int T = (p.t_from_len && L > 0 && L <= p.capacity) ? max(64, plan_t_from_len(L, p.P)) : p.T;
     nP = (L + T - 1) / T;
@@ -81,10 +63,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 
   // wait until the split kernel's partials are complete and visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  const bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql || nP < 0;
+  bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql;
   if (blockIdx.x == 0 && h == 0 && tid == 0) {  // report invalid lengths once per sequence
     if (L < 0 || L > p.capacity) atomicOr(p.status, VAE4_STATUS_BAD_LENGTH);
     else if (ql < 0 || ql > p.Qmax || (L > 0 && ql > L)) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
+  }
+  if (p.dev_plan && !dead) {
+    // the device-side plan, as the split kernel's CTA of the stream's first
+    // partition recorded it (every live row's stream has one)
+    const int2 e = p.plan_tab[b * p.Hkv + h];
+    slot0 = e.x;
+    nP = e.y;
+    if (slot0 < 0 || nP < 1 || nP > p.P || slot0 + nP > p.plan_G) {  // never: a library bug
+      if (tid == 0) atomicOr(p.status, VAE4_STATUS_PLAN);
+      dead = true;
+    }
   }
   if (dead) nP = 0;
   float *wm = csm;       // m_p, then the weight w_p
@@ -214,8 +207,7 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.Qmax * p.G * (p.D / 64), p.Hkv, p.B);
   cfg.blockDim = dim3(kCombineThreads);
-  // (m_p, l_p) per partition; with the device plan, (L, q_len) per sequence
-  cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float) + (p.dev_plan ? (size_t)p.B * 2 * sizeof(int) : 0);
+  cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float);  // (m_p, l_p) per partition
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

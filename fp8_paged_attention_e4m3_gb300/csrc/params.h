@@ -1,6 +1,7 @@
 // Launch parameters shared by the host entry points and the kernels.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace vae4 {
@@ -37,6 +38,7 @@ struct SplitParams {
   int32_t dev_plan;     // 1: partitions from the device-side balanced plan (grid.x = G)
   int32_t plan_G;       // device plan: CTAs along x = workspace slots
   int32_t plan_N;       // device plan: rows per CTA (a row group)
+  int2 *plan_tab;       // device plan: (first slot, partitions) [B][Hkv], for the combine
   int32_t plan_W_guess, plan_np_guess;  // device plan when every L is the capacity
   int32_t t_from_len;   // static grid: T = max(64, ceil16(L / P)) per sequence
 };
@@ -55,6 +57,7 @@ struct CombineParams {
   int32_t rows_pad, T, P, capacity;
   int32_t dev_plan, plan_G;  // device-side balanced plan and its CTA count
   int32_t plan_N;            // device plan: rows per split CTA
+  const int2 *plan_tab;      // device plan: (first slot, partitions) [B][Hkv]
   int32_t t_from_len;        // static grid, T from each sequence's length
   uint32_t *status;
 };

@@ -8,10 +8,10 @@
 // whatever the mix of lengths and query counts.  W starts at
 // ceil(sum r L / (G / Hkv)) rounded up to 16 and, if that does not fit, is
 // bisected (at most six steps) towards a bound that always fits.  At equal
-// lengths it is the static plan.  Partitions are numbered b-major, then h,
-// then p; partition x runs as CTAs (row group, x) of a (row groups) x G
-// grid, those of row groups without live queries leaving at once, and is
-// workspace slot x.  One warp evaluates the plan (lanes over sequences,
+// lengths it is the static plan.  Partitions are numbered by the sequence's
+// row groups (most first), then b, h, p; partition x runs as CTAs
+// (x, row group) of a G x (row groups) grid, those of row groups without
+// live queries leaving at once, and is workspace slot x.  One warp evaluates the plan (lanes over sequences,
 // B <= 1024).
 //
 // The arithmetic is written once, over a source of (live length, row
@@ -145,37 +145,51 @@ __device__ __forceinline__ int plan_width(const Len &len, int B, int Hkv, int G,
 struct PlanCta {
   int b, h, p;  // sequence, KV head, partition
   int W;        // the plan's partition length
+  int np;       // partitions of the stream
 };
 
+// Most row groups a sequence can keep busy (Qmax queries).
+__device__ __forceinline__ int plan_max_row_groups(const PlanIn &in) {
+  return (in.Qmax * in.gqa + in.N - 1) / in.N;
+}
+
 // Partition x -> (b, h, p); false if x is past the last partition.
+// Partitions are numbered by row groups (most first), then b, h, p: with
+// the row group as grid.y, the CTAs that row groups past the first keep
+// busy are the lowest x, launched first in their grid row.
 template <class Len>
-__device__ __forceinline__ bool plan_locate(const Len &len, int B, int Hkv, int W, int x, int lane,
-                                            PlanCta *out) {
-  int base = 0;  // partitions of the sequences before b0
-  for (int b0 = 0; b0 < B; b0 += 32) {
-    const int b = b0 + lane;
-    const int np = b < B ? (len(b).x + W - 1) / W : 0;
-    const int cnt = np * Hkv;
-    int incl = cnt;  // inclusive scan over the lanes
+__device__ __forceinline__ bool plan_locate(const Len &len, int B, int Hkv, int W, int rmax, int x,
+                                            int lane, PlanCta *out) {
+  int base = 0;  // partitions numbered before this chunk
+  for (int rc = rmax; rc >= 1; --rc) {
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      int2 v = make_int2(0, 0);
+      if (b < B) v = len(b);
+      const int np = v.y == rc ? (v.x + W - 1) / W : 0;
+      const int cnt = np * Hkv;
+      int incl = cnt;  // inclusive scan over the lanes
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int excl = incl - cnt;
+      const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && x >= base + excl && x < base + incl);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        const int e = __shfl_sync(0xffffffffu, excl, src);
+        const int n = __shfl_sync(0xffffffffu, np, src);
+        const int r = x - base - e;
+        const int hh = Hkv == 1 ? 0 : r / n;
+        out->b = b0 + src;
+        out->h = hh;
+        out->p = r - hh * n;
+        out->np = n;
+        return true;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    const int excl = incl - cnt;
-    const unsigned hit = __ballot_sync(0xffffffffu, cnt > 0 && x >= base + excl && x < base + incl);
-    if (hit) {
-      const int src = __ffs(hit) - 1;
-      const int e = __shfl_sync(0xffffffffu, excl, src);
-      const int n = __shfl_sync(0xffffffffu, np, src);
-      const int r = x - base - e;
-      const int hh = Hkv == 1 ? 0 : r / n;
-      out->b = b0 + src;
-      out->h = hh;
-      out->p = r - hh * n;
-      return true;
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
   }
   return false;
 }
@@ -211,7 +225,7 @@ static __device__ __noinline__ void plan_stage(const PlanIn in, int *Ls, int lan
 // Partition x of a split launch (CTA column x, one CTA per row group), from
 // the staged pairs, with the plan's W; p = -1 past the end of the plan.
 static __device__ __noinline__ PlanCta plan_cta(const PlanIn in, const int *Ls, int x, int lane) {
-  PlanCta c{-1, -1, -1, 0};
+  PlanCta c{-1, -1, -1, 0, 0};
   int W;
   bool ok;
   if (in.B <= 32) {  // one sequence per lane, in registers
@@ -223,23 +237,24 @@ static __device__ __noinline__ PlanCta plan_cta(const PlanIn in, const int *Ls, 
     }
     const LenReg len{v};
     W = plan_width(len, in.B, in.Hkv, in.G, lane);
-    ok = plan_locate(len, in.B, in.Hkv, W, x, lane, &c);
+    ok = plan_locate(len, in.B, in.Hkv, W, plan_max_row_groups(in), x, lane, &c);
   } else {
     const LenStaged len{Ls, in.Qmax, in.capacity, in.gqa, in.N};
     W = plan_width(len, in.B, in.Hkv, in.G, lane);
-    ok = plan_locate(len, in.B, in.Hkv, W, x, lane, &c);
+    ok = plan_locate(len, in.B, in.Hkv, W, plan_max_row_groups(in), x, lane, &c);
   }
-  if (!ok) c = PlanCta{-1, -1, -1, 0};
+  if (!ok) c = PlanCta{-1, -1, -1, 0, 0};
   c.W = W;
   return c;
 }
 
 // Same, with lengths read from global memory on every pass.
 static __device__ __noinline__ PlanCta plan_cta_global(const PlanIn in, int x, int lane) {
-  PlanCta c{-1, -1, -1, 0};
+  PlanCta c{-1, -1, -1, 0, 0};
   const LenGlobal len{in};
   const int W = plan_width(len, in.B, in.Hkv, in.G, lane);
-  if (!plan_locate(len, in.B, in.Hkv, W, x, lane, &c)) c = PlanCta{-1, -1, -1, 0};
+  if (!plan_locate(len, in.B, in.Hkv, W, plan_max_row_groups(in), x, lane, &c))
+    c = PlanCta{-1, -1, -1, 0, 0};
   c.W = W;
   return c;
 }
@@ -251,10 +266,14 @@ static __device__ __noinline__ int2 plan_stream_slots(const PlanIn in, const int
                                                       int lane) {
   const LenStaged len{Ls, in.Qmax, in.capacity, in.gqa, in.N};
   const int W = plan_width(len, in.B, in.Hkv, in.G, lane);
-  int before = 0;
-  for (int b1 = lane; b1 < b; b1 += 32) before += (len(b1).x + W - 1) / W;
+  const int2 vb = len(b);
+  int before = 0;  // partitions numbered before (b, 0, 0): more row groups, or as many and b1 < b
+  for (int b1 = lane; b1 < in.B; b1 += 32) {
+    const int2 v = len(b1);
+    if (v.y > vb.y || (v.y == vb.y && b1 < b)) before += (v.x + W - 1) / W;
+  }
   before = warp_sum_i(before);
-  int np = (len(b).x + W - 1) / W;
+  int np = (vb.x + W - 1) / W;
   const int s0 = before * in.Hkv + h * np;
   if (s0 + np > in.G) np = -1;
   return make_int2(s0, np);

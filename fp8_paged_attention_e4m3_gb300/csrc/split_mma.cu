@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(192, 1) split_mma_kernel(const SplitParams p) 
     part = c.p;
     T = c.W;
     pslot = blockIdx.x;
+    if (part == 0 && tid == 0) p.plan_tab[b * p.Hkv + h] = make_int2((int)blockIdx.x, c.np);
   } else {
     part = blockIdx.x;
     h = blockIdx.y;

@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
   // ---- which partition: static grid (partition, head x row group,
-  // sequence) or the device-side plan (grid.x = row group, grid.y =
-  // partition number).
+  // sequence) or the device-side plan (grid.x = partition number, grid.y =
+  // row group).
   // producers: first block-table window, requested as early as possible.
   // Lane l holds logical page lp_base + l (cur) and lp_base + 32 + l (nxt);
   // entries past the row are -1, entries past the sequence are loaded but
@@ -254,8 +254,8 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     // stream), which is the plan whenever the lengths are the capacity, and
     // fetch again if not.
     const int npg = p.plan_np_guess;
-    const int xs = (int)blockIdx.y / npg;  // stream of the guess
-    const int bg = xs / p.Hkv, k0g = ((int)blockIdx.y - xs * npg) * p.plan_W_guess;
+    const int xs = (int)blockIdx.x / npg;  // stream of the guess
+    const int bg = xs / p.Hkv, k0g = ((int)blockIdx.x - xs * npg) * p.plan_W_guess;
     if (bg < p.B) fetch_bt(bg, k0g);
     // The K producer warp evaluates the plan and passes it on through the
     // P^T buffer, unused until the first tile: the (L, q_len) pairs of the
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
       const PlanIn pin{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv,
                        p.plan_G, p.G, N};
       plan_stage(pin, plan_ls, lane);
-      const PlanCta c = plan_cta(pin, plan_ls, blockIdx.y, lane);
+      const PlanCta c = plan_cta(pin, plan_ls, blockIdx.x, lane);
       if (lane == 0) {
         plan_sh[0] = c.b;
         plan_sh[1] = c.h;
@@ -276,6 +276,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
         plan_sh[3] = c.W;
         plan_sh[4] = c.p >= 0 ? plan_ls[2 * c.b] : 0;
         plan_sh[5] = c.p >= 0 ? plan_ls[2 * c.b + 1] : 0;
+        // the stream's first slot and partition count, for the combine
+        if (c.p == 0 && blockIdx.y == 0)
+          p.plan_tab[c.b * p.Hkv + c.h] = make_int2((int)blockIdx.x, c.np);
       }
     }
     __syncthreads();
@@ -308,9 +311,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   // row group and workspace slot, from the CTA index alone (cheap to
   // recompute where they are needed, in the epilogue)
   constexpr bool DEV = MODE == kPlanDevice;
-  auto cta_rg = [&]() -> int { return DEV ? (int)blockIdx.x : (int)(blockIdx.y % a.n_rg); };
+  auto cta_rg = [&]() -> int { return DEV ? (int)blockIdx.y : (int)(blockIdx.y % a.n_rg); };
   auto cta_slot = [&]() -> int64_t {
-    return DEV ? (int64_t)blockIdx.y
+    return DEV ? (int64_t)blockIdx.x
                : ((int64_t)blockIdx.z * p.Hkv + blockIdx.y / a.n_rg) * p.P + blockIdx.x;
   };
   const int row0 = cta_rg() * N;  // first row of this CTA's row group
@@ -845,10 +848,10 @@ cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &
   // kernel on the stream drains; the kernel waits for it before its first
   // global-memory access that depends on it
   cudaLaunchConfig_t cfg = {};
-  // device plan: (row group, partition), so that the row groups of a
-  // partition are launched together and the CTAs of row groups without live
-  // queries (which leave at once) do not hold back later partitions
-  cfg.gridDim = MODE == kPlanDevice ? dim3(a.n_rg, p.plan_G, 1) : dim3(p.P, p.Hkv * a.n_rg, p.B);
+  // device plan: (partition, row group); the plan numbers the partitions of
+  // sequences with more live row groups first, so every live CTA of the
+  // second grid row comes before the ones that leave at once
+  cfg.gridDim = MODE == kPlanDevice ? dim3(p.plan_G, a.n_rg, 1) : dim3(p.P, p.Hkv * a.n_rg, p.B);
   cfg.blockDim = dim3(C::NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;

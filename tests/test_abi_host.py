@@ -75,7 +75,8 @@ def test_workspace_matches_the_pages_max_sum_layout():
     ml *= g["element_bytes"]
     assert ml - g["delta_bytes"] == 80 * 8 * 6 * 4            # the old [80,8,6]
     o = P * q * G * D * 4                                     # FP32 unnormalised PV
-    assert n == 256 + ml + o                                  # status + (max,sum) + PV
+    # status + (max,sum) + PV + (first slot, partitions) of the one stream
+    assert n == 256 + ml + o + 8
     qc = GOLD["q_copy"]
     assert qc["shape"][0] * qc["shape"][1] * qc["shape"][2] * qc["element_bytes"] == qc["max_bytes"]
 
