@@ -328,7 +328,33 @@ def main():
         g_br.replay()
     torch.cuda.synchronize()
     bridge_us = timed(g_br) * 1e3 / NB
-    del ko, vo
+    del ko, vo, g_br
+    # ---- ragged batch on the automatic plan (the device-side balanced plan):
+    # 16 sequences of log-uniform lengths and mixed query counts in a launch
+    # sized for the longest context, steps graph-replayed like the main leg
+    wr = W.generate("rag")
+    rq, rkv, rbt, rseq, rsc = W.to_device(wr, device=dev)
+    RR = max(2, math.ceil(3 * l2 / rkv.numel()))
+    rkvs = [rkv] + [rkv.clone() for _ in range(RR - 1)]
+    rout = torch.zeros_like(rq)
+    rs = wr.spec
+    rws = vae4.alloc_workspace(rs.B, rs.Hq, rs.Hkv, rs.Qmax, rs.D, wr.capacity, 0, device=dev)
+    rkw = dict(partition_tokens=0, max_seq_len=wr.capacity)
+    with torch.cuda.stream(stream):
+        vae4.verify(rq, rkvs[0], rbt, rseq, rsc, rout, rws, **rkw)
+    stream.synchronize()
+    NRG = max(3, min(20, args.steps))
+    g_rag = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_rag, stream=stream):
+        for k in range(NRG):
+            vae4.verify(rq, rkvs[k % RR], rbt, rseq, rsc, rout, rws, **rkw)
+    with torch.cuda.stream(stream):
+        g_rag.replay()
+    torch.cuda.synchronize()
+    rag_us = timed(g_rag) * 1e3 / NRG
+    assert vae4.read_status(rws) == 0
+    rag_bytes = wr.kv_bytes
+    del rkvs, rkv, rws, g_rag
     clocks = sampler.stop()
     split_mean_us = split_total_ms * 1e3 / args.steps
     step_med, step_p90 = float(np.median(samp["a"])), float(np.percentile(samp["a"], 90))
@@ -382,6 +408,7 @@ def main():
             "data": "synthetic",
             "config": {"workload": workload_desc(w), "seed": s.seed,
                        "partition_tokens": T_eff, "partitions": P,
+                       "plan": "automatic (one sequence: T from its length on the device)",
                        "timing": f"{args.steps} steps in one CUDA graph replay",
                        "l2": f"inputs rotate over {R} KV pool copies of {pool_bytes >> 20} MiB "
                              f"(> 3x the {l2 >> 20} MiB L2)"},
@@ -410,6 +437,15 @@ def main():
                 "gbs": 3 * kv_bytes / (bridge_us * 1e-6) / 1e9,
                 "frac": 3 * kv_bytes / (bridge_us * 1e-6) / 1e9 / peak,
                 "timing": f"{NB} back-to-back launches in one CUDA graph"},
+            "ragged": {
+                "workload": (f"rag: B{rs.B} Qmax{rs.Qmax} q in {sorted(set(int(x) for x in wr.q_len))} "
+                             f"Hq{rs.Hq} Hkv{rs.Hkv} D{rs.D} L {int(wr.seq_len.min())}.."
+                             f"{int(wr.seq_len.max())} page{rs.page} capacity {wr.capacity}"),
+                "plan": "automatic: device-side balanced plan",
+                "us_per_step": rag_us, "kv_bytes": rag_bytes,
+                "gbs": rag_bytes / (rag_us * 1e-6) / 1e9,
+                "frac": rag_bytes / (rag_us * 1e-6) / 1e9 / peak,
+                "timing": f"{NRG} steps in one CUDA graph replay, KV rotating over {RR} pool copies"},
             "gpu_launches": gpu_launches,
             "clocks": clocks,
             "gpu": props.name,
