@@ -15,9 +15,10 @@
 // B <= 1024).
 //
 // The arithmetic is written once, over a source of (live length, row
-// groups) pairs: the split kernel stages the lengths in shared memory, the
-// combine reads global memory; the same lengths give every kernel the same
-// plan.
+// groups) pairs: the tcgen05 split kernel stages the lengths in shared
+// memory, the mma.sync one reads global memory.  The CTA of each stream's
+// first partition records the stream's first slot and partition count in
+// the workspace for the combine.
 #pragma once
 
 #include <stdint.h>
@@ -257,26 +258,6 @@ static __device__ __noinline__ PlanCta plan_cta_global(const PlanIn in, int x, i
     c = PlanCta{-1, -1, -1, 0, 0};
   c.W = W;
   return c;
-}
-
-// Stream (b, h) -> (first slot, partition count), from the staged pairs;
-// the count is -1 if the stream's slots would run past the grid (never: the
-// plan fits by construction).
-static __device__ __noinline__ int2 plan_stream_slots(const PlanIn in, const int *Ls, int b, int h,
-                                                      int lane) {
-  const LenStaged len{Ls, in.Qmax, in.capacity, in.gqa, in.N};
-  const int W = plan_width(len, in.B, in.Hkv, in.G, lane);
-  const int2 vb = len(b);
-  int before = 0;  // partitions numbered before (b, 0, 0): more row groups, or as many and b1 < b
-  for (int b1 = lane; b1 < in.B; b1 += 32) {
-    const int2 v = len(b1);
-    if (v.y > vb.y || (v.y == vb.y && b1 < b)) before += (v.x + W - 1) / W;
-  }
-  before = warp_sum_i(before);
-  int np = (vb.x + W - 1) / W;
-  const int s0 = before * in.Hkv + h * np;
-  if (s0 + np > in.G) np = -1;
-  return make_int2(s0, np);
 }
 
 }  // namespace vae4

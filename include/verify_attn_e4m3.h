@@ -138,8 +138,8 @@ enum vae4_error {
 #define VAE4_STATUS_BAD_LENGTH 0x2u /* L < 0 or L > launch capacity */
 #define VAE4_STATUS_BAD_QLEN 0x4u   /* q_len < 0, q_len > Qmax, or q_len > L > 0 */
 #define VAE4_STATUS_TIMEOUT 0x8u    /* a bounded pipeline wait ran out */
-#define VAE4_STATUS_PLAN 0x10u      /* the device-side partition plan overran the grid
-                                       (an internal invariant; the rows are zeroed) */
+#define VAE4_STATUS_PLAN 0x10u      /* a stream's record of the device-side plan is out of
+                                       range (an internal invariant; the rows are zeroed) */
 
 /*
  * verify_attn_e4m3 -- the verify step (split kernel + combine kernel).
@@ -274,12 +274,15 @@ int verify_attn_e4m3_kv_read(const vae4_tensor *q, const vae4_tensor *kv_pages,
  * (so a captured graph stays balanced as the lengths change):
  *  - B == 1 (or B > 1024): each sequence keeps the P partitions above and
  *    takes T = max(64, ceil(L / P) rounded up to 16) from its own L;
- *  - 1 < B <= 1024: the device-side balanced plan.  One length W, a
- *    multiple of 16 and at least 64, for every (sequence, KV head) stream,
- *    P_b = ceil(L_b / W), with sum_b Hkv * P_b <= G = max(num_sms, B*Hkv),
- *    W from ceil(sum L / (G / Hkv)) and at most six bisection steps; the
- *    partitions, numbered sequence-major, then KV head, then partition,
- *    run as G CTAs (times the row groups) in one wave.
+ *  - 1 < B <= 1024 (and B*Hkv*row groups <= 65535): the device-side
+ *    balanced plan.  One length W, a multiple of 16 and at least 64, for
+ *    every (sequence, KV head) stream, P_b = ceil(L_b / W) partitions, each
+ *    run by r_b CTAs, one per row group of the split kernel holding a live
+ *    query (r_b = ceil(q_len * Hq/Hkv / rows per CTA)), with
+ *    sum_b Hkv * r_b * P_b <= G = max(num_sms, B*Hkv*row groups): W from
+ *    ceil(sum r L / (G / Hkv)) and at most six bisection steps.  All live
+ *    CTAs run in one wave; partitions are numbered by r_b (largest first),
+ *    then sequence, KV head and partition.
  * Both give the same results as any fixed T up to FP32 rounding order.
  */
 int verify_attn_e4m3_plan(int B, int Hkv, int max_seq_len, int partition_tokens,
@@ -293,7 +296,9 @@ int verify_attn_e4m3_plan(int B, int Hkv, int max_seq_len, int partition_tokens,
  * final status) and the FP32 unnormalised P.V per partition and row
  * ([B][Hkv][P][rows][D]); rows = Qmax * Hq/Hkv rounded up to 16.  With
  * partition_tokens == 0 and 1 < B <= 1024 the partials take
- * max(B*Hkv*P, num_sms, B*Hkv) slots of [rows] (the device plan's grid).
+ * max(B*Hkv*P, num_sms, B*Hkv*row groups) slots of [rows] (the device
+ * plan's grid); a final B*Hkv*8 bytes hold each stream's (first slot,
+ * partitions) under that plan.
  * num_sms == 0 queries the current device (a CUDA call); any other value
  * makes this a pure host computation.  Returns the size, or a negative
  * vae4_error.
