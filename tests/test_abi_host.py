@@ -81,6 +81,33 @@ def test_workspace_matches_the_pages_max_sum_layout():
     assert qc["shape"][0] * qc["shape"][1] * qc["shape"][2] * qc["element_bytes"] == qc["max_bytes"]
 
 
+def test_workspace_of_the_device_plan():
+    """Automatic plans of a batch (1 < B <= 1024) size the partials for the
+    device-side plan's grid, max(B*Hkv*P, SMs, B*Hkv*row groups) slots, plus
+    8 bytes per (sequence, KV head) stream for the stream table; one
+    sequence and explicit partition lengths keep the static B*Hkv*P."""
+    def layout(slots, rows_pad, D, streams):
+        al = lambda x: (x + 255) // 256 * 256
+        o_off = al(256 + slots * rows_pad * 2 * 4)
+        return al(o_off + slots * rows_pad * D * 4) + streams * 8
+
+    # ragged shape: 16 sequences, q16 x GQA6 = 96 rows in two row groups of 48
+    B, Hq, Hkv, Qmax, D, cap = 16, 6, 1, 16, 256, 262144
+    T, P = vae4.plan(B, Hkv, cap, 0, 152)
+    slots = max(B * Hkv * P, 152, B * Hkv * 2)
+    assert vae4.workspace_bytes(B, Hq, Hkv, Qmax, D, cap, 0, 152) == layout(slots, 96, D, B * Hkv)
+    # more streams than SMs: the grid covers one CTA per (stream, row group)
+    B, Hkv, Hq = 100, 2, 12
+    T, P = vae4.plan(B, Hkv, cap, 0, 152)
+    slots = max(B * Hkv * P, 152, B * Hkv * 2)
+    assert vae4.workspace_bytes(B, Hq, Hkv, Qmax, D, cap, 0, 152) == layout(slots, 96, D, B * Hkv)
+    # one sequence (length-derived T on the static grid), an explicit T, and a
+    # batch above the device plan's limit: the static slot count
+    for B, T_req in ((1, 0), (16, 2048), (1025, 0)):
+        T, P = vae4.plan(B, 1, cap, T_req, 152)
+        assert vae4.workspace_bytes(B, 6, 1, 8, D, cap, T_req, 152) == layout(B * P, 48, D, B)
+
+
 def test_workspace_errors():
     with pytest.raises(vae4.Vae4Error):
         vae4.workspace_bytes(1, 6, 4, 8, 256, 1000, 0, 152)   # GQA mismatch
