@@ -186,7 +186,10 @@ def verify_attn_e4m3(q, kv_pages, block_table, seq_lens, kv_scales, out, workspa
                      max_seq_len: int = 0, num_sms: int = 0, flags: int = 0, stream=None):
     """Run the verify step into ``out``.  All tensors on the current device;
     see include/verify_attn_e4m3.h for layouts.  Asynchronous on ``stream``
-    (torch's current stream by default)."""
+    (torch's current stream by default).  ``partition_tokens=0`` selects the
+    automatic plan, made on the device from the lengths of each call (a
+    captured graph stays balanced as they change); a positive multiple of 16
+    fixes T."""
     lib = load()
     opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
                   int(num_sms), int(flags))
@@ -266,7 +269,9 @@ def verify_attn_e4m3_noalloc(q, kv_pages, block_table, seq_lens, kv_scales, out,
 
 def verify_attn_e4m3_plan(B: int, Hkv: int, max_seq_len: int, partition_tokens: int = 0,
                           num_sms: int = 0):
-    """(T, P) of the split-K plan; num_sms == 0 uses the current device."""
+    """(T, P) of the split-K plan for sequences at the capacity (with
+    partition_tokens == 0 a call refines it on the device from the lengths it
+    reads); num_sms == 0 uses the current device."""
     lib = load()
     if num_sms == 0:
         import torch
