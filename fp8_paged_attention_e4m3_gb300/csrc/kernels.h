@@ -9,6 +9,12 @@
 
 namespace vae4 {
 
+// Unique id of the CUDA context current on the calling thread (0 if none
+// is current or the driver cannot tell).  Per-device caches of the host
+// code (function attributes, symbol addresses) are keyed on it, so that a
+// context created after cudaDeviceReset is set up afresh.
+unsigned long long current_context_id();
+
 // Split kernel on the warp-level (mma.sync) tensor-core path.
 size_t split_mma_smem_bytes(int D, int rows_pad);
 int split_mma_threads(int rows_pad);

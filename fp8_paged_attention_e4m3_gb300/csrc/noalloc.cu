@@ -9,6 +9,7 @@
 
 #include <mutex>
 
+#include "kernels.h"
 #include "verify_attn_e4m3.h"
 
 namespace {
@@ -21,17 +22,21 @@ static __device__ __align__(256) unsigned char g_scratch[VAE4_NOALLOC_SCRATCH_BY
 constexpr int kMaxDevices = 128;
 std::mutex g_mu;
 void *g_addr[kMaxDevices] = {nullptr};
+unsigned long long g_ctx[kMaxDevices] = {0};  // context the address belongs to
 
 // Device address of the scratch on the current device, looked up on first
-// use (with that device current) and cached.
+// use (with that device current) and cached for the device's context; a
+// new context (after cudaDeviceReset) gets a fresh lookup.
 int scratch_address(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VAE4_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  const unsigned long long ctx = vae4::current_context_id();
+  if (!g_addr[dev] || ctx == 0 || ctx != g_ctx[dev]) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return VAE4_ERR_CUDA;
     g_addr[dev] = p;
+    g_ctx[dev] = vae4::current_context_id();  // the lookup made the context current
   }
   *out = g_addr[dev];
   return VAE4_OK;

@@ -59,6 +59,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "kernels.h"
 #include "params.h"
 #include "plan.cuh"
 #include "tc_ptx.cuh"
@@ -556,6 +557,14 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
         if (!tc::mbar_wait(bar(kVFull + st), (t / C::NVR) & 1, abort_f, LIM)) break;
         tc::tc_fence_after();
         const uint32_t rawV = sVR + st * C::RSLOT;
+        // The box holding key k1 - 1 is loaded whole, so up to 15 of its
+        // keys lie past the partition.  When k1 = L those pool slots may
+        // never have been written (a NaN or infinity code there would turn
+        // the masked key's P = 0 into a NaN product), so their bytes are
+        // zeroed here; boxes that start at or past k1 are zero-filled by the
+        // copy itself.
+        const int kb = k0 + 64 * t;  // first key of the half-tile
+        const bool edge = kb + 64 > k1;
 #pragma unroll
         for (int mh = 0; mh < C::MH; ++mh) {
 #pragma unroll
@@ -571,6 +580,14 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
                 ldsm_b8_trans_x2(m4, src + (2 * kp + pg) * (16 * D));
                 // m4[0]: keys 4(l%4) + 0..3 of d = l/4, m4[1]: of d + 8;
                 // m4[2], m4[3]: the same for the keys 16 later
+                if (edge) {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int kq = kb + 32 * kp + 16 * (e >> 1) + 4 * (lane & 3);
+                    const int nv = min(max(k1 - kq, 0), 4);  // bytes (keys) before k1
+                    m4[e] &= nv >= 4 ? 0xFFFFFFFFu : ((1u << (8 * nv)) - 1u);
+                  }
+                }
                 uint32_t v[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -833,16 +850,20 @@ template <int D, int N, int MODE>
 cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &map,
                       cudaStream_t stream) {
   using C = TcCfg<D, N>;
-  // the shared-memory opt-in is a per-device function attribute: set it once
-  static std::atomic<uint64_t> configured{0};
+  // the shared-memory opt-in is a function attribute of the device's
+  // context: set it once per context (a context made after cudaDeviceReset
+  // starts without it)
+  constexpr int kDevs = 64;
+  static std::atomic<unsigned long long> configured[kDevs] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-  const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
-  if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+  const unsigned long long ctx = current_context_id();
+  if (dev < 0 || dev >= kDevs || ctx == 0 ||
+      configured[dev].load(std::memory_order_acquire) != ctx) {
     cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<D, N, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_acq_rel);
+    if (dev >= 0 && dev < kDevs) configured[dev].store(current_context_id(), std::memory_order_release);
   }
   // programmatic dependent launch: the CTAs may be placed while the previous
   // kernel on the stream drains; the kernel waits for it before its first

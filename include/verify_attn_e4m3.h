@@ -156,6 +156,9 @@ enum vae4_error {
  *              PR #560, Purpose and Test Plan and Results; PR #524, AI
  *              review); base 16-byte aligned.  Each (page, K|V, head) slice
  *              of page*D bytes is one contiguous 16-byte-aligned block.
+ *              Slots past L in a sequence's last page may hold anything
+ *              (e.g. never written, NaN codes): they do not reach the
+ *              output.
  *  block_table I32 [B][max_pages], stride[1] == 1: logical page j of
  *              sequence b lives in physical page block_table[b][j].  The ids
  *              of the first ceil(L/page) entries of a row are used; up to 64
@@ -360,8 +363,9 @@ int verify_attn_e4m3_decode_table(void *dev_out, int32_t *scale_log2, int32_t fl
  * cudaFree, no allocating library routine.
  *
  *  - The first call on a device looks up the scratch array's device
- *    address (once per device, with that device current).  Make that first
- *    call before any stream capture on the device.
+ *    address (once per device, with that device current; again after
+ *    cudaDeviceReset, which makes a new context).  Make that first call
+ *    before any stream capture on the device.
  *  - A call whose partition plan needs more than VAE4_NOALLOC_SCRATCH_BYTES
  *    (see verify_attn_e4m3_workspace_bytes) returns VAE4_ERR_WORKSPACE and
  *    launches nothing.  Example sizes: the 262144-token q8 GQA6 D256 step

@@ -399,3 +399,70 @@ def test_single_sequence_auto_plan_below_capacity(L):
     compare(gpu, ref, live)
     assert not gpu[~live].any()
     assert vae4.read_status(ws) == 0
+
+
+# ------------------------------------------- unwritten pool slots past L
+def _poison_past_l(w, codes):
+    """Fill every pool byte of the slots past L in each sequence's last page
+    (K and V, all heads) with the given codes in turn: slots a real cache
+    may never have written.  The oracle reads keys < L only."""
+    page = w.spec.page
+    k = 0
+    for b in range(w.spec.B):
+        L = int(w.seq_len[b])
+        if L == 0 or L % page == 0:
+            continue
+        phys = int(w.block_table[b, (L - 1) // page])
+        for slot in range(L % page, page):
+            w.kv_pages[phys, :, :, slot, :] = codes[k % len(codes)]
+            k += 1
+    assert k > 0
+    return w
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[1000, 37], q_lens=[8, 8], seed=70,
+         partition_tokens=256),
+    dict(B=1, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[20001], q_lens=[8], seed=71),
+    dict(B=3, Qmax=16, Hq=6, Hkv=1, D=256, seq_lens=[5003, 999, 70], q_lens=[16, 8, 1],
+         seed=72),
+    dict(B=1, Qmax=8, Hq=2, Hkv=1, D=64, seq_lens=[1000], q_lens=[8], seed=73, page=48,
+         partition_tokens=512),
+], ids=["T256", "auto-one", "auto-batch", "page48"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_nan_and_inf_codes_past_the_length_do_not_leak(cfg, fmt):
+    """A masked key has P = 0, but 0 * NaN is NaN: the split kernel must not
+    feed the bytes of unwritten slots past L into the value product."""
+    w = W.custom("poison", kv_format=fmt, **cfg)
+    codes = [0x7F, 0xFF] if fmt == "e4m3" else [0x7C, 0xFC, 0x7F, 0xFF]
+    check_full(_poison_past_l(w, codes))
+
+
+# --------------------------------------------- the plain 8-argument call
+def test_plain_entry_point_matches_ex_with_defaults():
+    """verify_attn_e4m3 (the eight-argument form) is verify_attn_e4m3_ex with
+    default options: automatic plan, capacity = block-table columns x page,
+    1/sqrt(D).  Same bits, and within the bar against the oracle."""
+    import ctypes
+    lib = vae4.load()
+    w = W.custom("plain", B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[7000, 3297],
+                 q_lens=[8, 5], seed=74)
+    q, kv, bt, seq, sc = W.to_device(w)
+    s = w.spec
+    cap = w.block_table.shape[1] * s.page
+    ws = vae4.alloc_workspace(s.B, s.Hq, s.Hkv, s.Qmax, s.D, cap, 0)
+    outs = []
+    for plain in (True, False):
+        out = torch.full_like(q, float("nan"))
+        d = [vae4.describe(t) for t in (q, kv, bt, seq, sc, out, ws)]
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        if plain:
+            rc = lib.verify_attn_e4m3(*[ctypes.byref(x) for x in d], st)
+        else:
+            rc = lib.verify_attn_e4m3_ex(*[ctypes.byref(x) for x in d], st, None)
+        assert rc == 0
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    compare(outs[0], oracle_full(w))
+    assert vae4.read_status(ws) == 0

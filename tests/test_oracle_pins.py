@@ -262,3 +262,20 @@ def test_bad_block_id_is_reported():
     w.block_table[0, 1] = w.kv_pages.shape[0]
     with pytest.raises(oracle.OracleError):
         _run(w)
+
+
+def test_length_beyond_the_block_table_is_reported():
+    """L past the last token the block table can address (max_pages * page)
+    is an input error, reported rather than read out of bounds; L exactly at
+    that limit is valid and gives the same rows as a wider table."""
+    w = _small(B=2, seq_lens=[40, 5], q_lens=[1, 1])
+    cap = w.block_table.shape[1] * w.spec.page
+    sl = w.seq_len.copy()
+    sl[0] = cap + 1
+    with pytest.raises(oracle.OracleError, match="beyond the block table"):
+        oracle.verify_attn(w.q, w.kv_pages, w.block_table, sl, w.q_len, w.kv_scales)
+    sl[0] = cap
+    wide = np.concatenate([w.block_table, np.full_like(w.block_table, -1)], axis=1)
+    a = oracle.verify_attn(w.q, w.kv_pages, w.block_table, sl, w.q_len, w.kv_scales)
+    b = oracle.verify_attn(w.q, w.kv_pages, wide, sl, w.q_len, w.kv_scales)
+    assert np.array_equal(a, b) and np.isfinite(a).all()

@@ -348,6 +348,17 @@ def midpoint_case(n: int = 1024, D: int = 64) -> Workload:
     return w
 
 
+def relocate(w: Workload, seed: int) -> Workload:
+    """The same logical cache with every physical page moved to a seeded
+    random place in the pool: the pages and the block table are permuted
+    together, so every sequence reads the same bytes from other addresses."""
+    perm = _rng(seed, 4242).permutation(w.kv_pages.shape[0]).astype(np.int32)
+    kv = np.empty_like(w.kv_pages)
+    kv[perm] = w.kv_pages  # page p moves to perm[p]
+    bt = np.where(w.block_table >= 0, perm[np.maximum(w.block_table, 0)], -1)
+    return dataclasses.replace(w, kv_pages=kv, block_table=bt.astype(np.int32))
+
+
 def to_device(w: Workload, device="cuda", seq_len=None, q_len=None):
     """The workload's inputs as device tensors for the library:
     (q, kv_pages, block_table, seq_lens [B][2] = (L, q_len), kv_scales)."""
