@@ -12,7 +12,7 @@ import ctypes
 import os
 import threading
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 VAE4_U8, VAE4_I32, VAE4_F16, VAE4_F32 = 1, 2, 3, 4
 
@@ -59,7 +59,7 @@ class Options(ctypes.Structure):
     """vae4_options"""
     _fields_ = [("softmax_scale", ctypes.c_float), ("partition_tokens", ctypes.c_int32),
                 ("max_seq_len", ctypes.c_int32), ("num_sms", ctypes.c_int32),
-                ("flags", ctypes.c_int32)]
+                ("flags", ctypes.c_int32), ("hilo_pv", ctypes.c_int32)]
 
 
 class Vae4Error(RuntimeError):
@@ -183,16 +183,18 @@ def _check(rc: int, where: str):
 # ----------------------------------------------------------------------------
 def verify_attn_e4m3(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, *,
                      softmax_scale: float = 0.0, partition_tokens: int = 0,
-                     max_seq_len: int = 0, num_sms: int = 0, flags: int = 0, stream=None):
+                     max_seq_len: int = 0, num_sms: int = 0, flags: int = 0,
+                     hilo_pv: bool = False, stream=None):
     """Run the verify step into ``out``.  All tensors on the current device;
     see include/verify_attn_e4m3.h for layouts.  Asynchronous on ``stream``
     (torch's current stream by default).  ``partition_tokens=0`` selects the
     automatic plan, made on the device from the lengths of each call (a
     captured graph stays balanced as they change); a positive multiple of 16
-    fixes T."""
+    fixes T.  ``hilo_pv=True`` carries P into the value product as an FP16
+    high part plus a residual scaled by 2^11 (about 22 significant bits)."""
     lib = load()
     opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
-                  int(num_sms), int(flags))
+                  int(num_sms), int(flags), int(bool(hilo_pv)))
     descs = [describe(t) for t in (q, kv_pages, block_table, seq_lens, kv_scales, out,
                                    workspace)]
     rc = lib.verify_attn_e4m3_ex(*[ctypes.byref(x) for x in descs],
@@ -206,10 +208,10 @@ verify = verify_attn_e4m3
 
 def _stage(name, q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, *,
            softmax_scale=0.0, partition_tokens=0, max_seq_len=0, num_sms=0, flags=0,
-           stream=None):
+           hilo_pv=False, stream=None):
     lib = load()
     opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
-                  int(num_sms), int(flags))
+                  int(num_sms), int(flags), int(bool(hilo_pv)))
     descs = [describe(t) for t in (q, kv_pages, block_table, seq_lens, kv_scales, out,
                                    workspace)]
     rc = getattr(lib, name)(*[ctypes.byref(x) for x in descs],
@@ -251,14 +253,15 @@ def verify_attn_e4m3_kv_read(*args, **kw):
 
 def verify_attn_e4m3_noalloc(q, kv_pages, block_table, seq_lens, kv_scales, out, *,
                              softmax_scale: float = 0.0, partition_tokens: int = 0,
-                             max_seq_len: int = 0, num_sms: int = 0, stream=None):
+                             max_seq_len: int = 0, num_sms: int = 0, hilo_pv: bool = False,
+                             stream=None):
     """The verify step without a workspace, for callers that cannot allocate
     device memory: the library's own fixed 8 MiB scratch holds the partials.
     Calls on one device share that scratch, so they must not overlap on the
     GPU; the first call on a device must precede any stream capture."""
     lib = load()
     opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
-                  int(num_sms), 0)
+                  int(num_sms), 0, int(bool(hilo_pv)))
     descs = [describe(t) for t in (q, kv_pages, block_table, seq_lens, kv_scales, out)]
     rc = lib.verify_attn_e4m3_noalloc(*[ctypes.byref(x) for x in descs],
                                       ctypes.c_void_p(_stream_handle(stream)),

@@ -175,7 +175,9 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   if (opt) o = *opt;
   if ((o.flags & ~(VAE4_FLAG_WARP_MMA | VAE4_FLAG_KV_E5M2 | VAE4_FLAG_TEST_SHORT_WAITS)) != 0)
     return VAE4_ERR_OPTIONS;
-  if ((o.flags & VAE4_FLAG_WARP_MMA) && (o.flags & (VAE4_FLAG_KV_E5M2 | VAE4_FLAG_TEST_SHORT_WAITS)))
+  if (o.hilo_pv != 0 && o.hilo_pv != 1) return VAE4_ERR_OPTIONS;
+  if ((o.flags & VAE4_FLAG_WARP_MMA) &&
+      ((o.flags & (VAE4_FLAG_KV_E5M2 | VAE4_FLAG_TEST_SHORT_WAITS)) || o.hilo_pv))
     return VAE4_ERR_UNSUPPORTED;
 
   int rc = check_qo(q);
@@ -317,6 +319,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   s.capacity = (int32_t)cap;
   s.sm_scale = sm_scale;
   s.kv_e5m2 = (o.flags & VAE4_FLAG_KV_E5M2) ? 1 : 0;
+  s.hilo = o.hilo_pv;
   s.dev_plan = dev_plan ? 1 : 0;
   s.t_from_len = t_from_len ? 1 : 0;
   s.plan_G = Gp;

@@ -41,6 +41,7 @@ struct SplitParams {
   int2 *plan_tab;       // device plan: (first slot, partitions) [B][Hkv], for the combine
   int32_t plan_W_guess, plan_np_guess;  // device plan when every L is the capacity
   int32_t t_from_len;   // static grid: T = max(64, ceil16(L / P)) per sequence
+  int32_t hilo;         // 1: P enters the value product as FP16 high + residual
 };
 
 // The combine kernel's parameters.

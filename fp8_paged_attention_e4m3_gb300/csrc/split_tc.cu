@@ -90,7 +90,8 @@ cudaError_t launch_split_tc(const SplitParams &p, long long wait_limit, cudaStre
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   if (p.dev_plan) return launch_split_tc_dev(p, a, n, map, stream);
   if (p.t_from_len) return launch_split_tc_len(p, a, n, map, stream);
-  return launch_tc_any<kPlanFixed>(p, a, n, map, stream);
+  return p.hilo ? launch_tc_any<kPlanFixed, true>(p, a, n, map, stream)
+                : launch_tc_any<kPlanFixed, false>(p, a, n, map, stream);
 }
 
 }  // namespace vae4

@@ -74,7 +74,7 @@ struct TcArgs {
   int32_t n_rg;          // row groups per KV head
 };
 
-template <int D, int N>
+template <int D, int N, bool HL = false>
 struct TcCfg {
   static_assert(N % 16 == 0 && N >= 16 && N <= 64, "rows per CTA");
   static constexpr int NSW = 8;                 // softmax warps
@@ -93,17 +93,18 @@ struct TcCfg {
   static constexpr int NVF = (512 - VCOL) / VTC < 4 ? (512 - VCOL) / VTC : 4;
   static constexpr int QB = (D / 64) * N * 128; // Q, K-major SW128
   static constexpr int PB = 128 * 128;          // P^T, MN-major SW128 (N <= 64)
+  static constexpr int NPB = HL ? 2 : 1;        // P^T buffers: P, or P_hi and P_lo
   static constexpr int RSLOT = 64 * D;          // one raw K or V half-tile
   static constexpr int SMALL = 2880;
   static constexpr int LIMIT = 232448 - 1024;   // opt-in maximum minus alignment slack
   // raw slots: whatever shared memory is left, split between the rings
   // (NVR >= NVF keeps the V decoders' slot waits unambiguous)
-  static constexpr int NRAW = (LIMIT - QB - PB - SMALL) / RSLOT;
+  static constexpr int NRAW = (LIMIT - QB - NPB * PB - SMALL) / RSLOT;
   static constexpr int NKR = NRAW / 2 < 8 ? NRAW / 2 : 8;
   static constexpr int NVR = NRAW - NKR < 8 ? NRAW - NKR : 8;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_P = OFF_Q + QB;
-  static constexpr int OFF_KR = OFF_P + PB;
+  static constexpr int OFF_KR = OFF_P + NPB * PB;
   static constexpr int OFF_VR = OFF_KR + NKR * RSLOT;
   static constexpr int OFF_SMALL = OFF_VR + NVR * RSLOT;
   static constexpr int SMEM = OFF_SMALL + SMALL + 1024;
@@ -140,16 +141,37 @@ constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmVotes = 544, kSmM
 
 __device__ __forceinline__ uint32_t sw128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
 
+// Zero the raw V bytes of keys kz .. 63 of a half-tile slot in the columns
+// V decoder warp dq reads (d = 128 mh + 32 dq + 0..31).  The slot was
+// written by the tensor copy (async proxy) and will be again after the
+// decoders release it, hence the proxy fence after the generic stores.
+template <int D, int IB, int SMASK, int MH>
+static __device__ __noinline__ void zero_v_tail(uint8_t *raw, int kz, int dq, int lane) {
+  constexpr int NG = 2 * MH;  // 16-byte column granules of the warp per key
+  for (int i = lane; i < (64 - kz) * NG; i += 32) {
+    const int k = kz + i / NG, g = i % NG;
+    const int dch = 128 * (g >> 1) + 32 * dq + 16 * (g & 1);
+    if (dch < D) {
+      const int dh = dch / IB, cc = (dch % IB) >> 4;
+      const uint32_t off = (uint32_t)((k & 15) * IB + cc * 16);
+      *reinterpret_cast<uint4 *>(raw + (k >> 4) * (16 * D) + dh * (16 * IB) +
+                                 (off ^ (((off >> 7) & SMASK) << 4))) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // Partition plans, one instantiation each so none carries another's code:
 // kPlanFixed: static grid (partition, head x row group, sequence), T given;
 // kPlanFromLen: static grid, T from each sequence's length (the automatic
 // plan of one sequence); kPlanDevice: the device-side balanced plan
 // (grid.x = partition number, grid.y = row group).
 enum { kPlanFixed = 0, kPlanFromLen = 1, kPlanDevice = 2 };
-template <int D, int N, int MODE>
-__global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
+template <int D, int N, int MODE, bool HL>
+__global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
     split_tc_kernel(const SplitParams p, const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
-  using C = TcCfg<D, N>;
+  using C = TcCfg<D, N, HL>;
   constexpr int kKFull = C::B_KFULL, kKEmpty = C::B_KEMPTY, kVFull = C::B_VFULL,
                 kVEmpty = C::B_VEMPTY, kKReady = C::B_KREADY, kKFree = C::B_KFREE,
                 kVReady = C::B_VREADY, kVFree = C::B_VFREE, kSFull = C::B_SFULL,
@@ -164,7 +186,16 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
   // O^T; with 30-sigma outliers 2^8 cost 3 us per step on the long q8 step,
   // 2^12 leaves 0.6 us, at a relative L2 error of 2.5e-4 instead of 2.2e-4
   // against the FP64 oracle (a wider P range inside each MMA).
-  constexpr float kTau = 12.0f;
+  // With the high/residual split of P (HL) the value product runs on P
+  // scaled by 2^11 (see the softmax), and 2^(4 + 11) keeps it inside FP16.
+  constexpr float kTau = HL ? 4.0f : 12.0f;
+  // HL: P' = 2^11 p is split into P_hi = fp16(P') and P_lo = fp16(P' -
+  // P_hi), i.e. the residual of fp16(p) multiplied by 2^11 (PR #524
+  // "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32 partials",
+  // Historical R6 purpose and evidence, Scope and non-duplication); both go
+  // through the value product into the same FP32 accumulator, and the exact
+  // 2^-11 is applied to O and l in the epilogue.
+  constexpr float kHiLoExp = HL ? 11.0f : 0.0f;
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
@@ -474,6 +505,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
               const uint32_t bp = sP + ks * 2048;
               tc::mma_ts(tbase + C::OCOL + mh * C::SC, av, tc::smem_desc(bp, 16384, 1024), id_pv,
                          (j > 0 || ks > 0) ? 1u : 0u);
+              if constexpr (HL)  // the residual, same V^T, same accumulator
+                tc::mma_ts(tbase + C::OCOL + mh * C::SC, av,
+                           tc::smem_desc(bp + C::PB, 16384, 1024), id_pv, 1u);
             }
           }
           tc::mma_commit(bar(kVFree + vs));
@@ -560,11 +594,13 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
         // The box holding key k1 - 1 is loaded whole, so up to 15 of its
         // keys lie past the partition.  When k1 = L those pool slots may
         // never have been written (a NaN or infinity code there would turn
-        // the masked key's P = 0 into a NaN product), so their bytes are
-        // zeroed here; boxes that start at or past k1 are zero-filled by the
-        // copy itself.
-        const int kb = k0 + 64 * t;  // first key of the half-tile
-        const bool edge = kb + 64 > k1;
+        // the masked key's P = 0 into a NaN product): this warp zeroes its
+        // columns of those keys (boxes that start at or past k1 are
+        // zero-filled by the copy itself).  Out of line, so the hot loop
+        // below keeps its code.
+        const int kz = k1 - k0 - 64 * t;  // keys of the half-tile before k1
+        if (kz > 0 && kz < 64 && (kz & 15) != 0)
+          zero_v_tail<D, C::IB, C::SMASK, C::MH>(gbase + C::OFF_VR + st * C::RSLOT, kz, dq, lane);
 #pragma unroll
         for (int mh = 0; mh < C::MH; ++mh) {
 #pragma unroll
@@ -580,14 +616,6 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
                 ldsm_b8_trans_x2(m4, src + (2 * kp + pg) * (16 * D));
                 // m4[0]: keys 4(l%4) + 0..3 of d = l/4, m4[1]: of d + 8;
                 // m4[2], m4[3]: the same for the keys 16 later
-                if (edge) {
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const int kq = kb + 32 * kp + 16 * (e >> 1) + 4 * (lane & 3);
-                    const int nv = min(max(k1 - kq, 0), 4);  // bytes (keys) before k1
-                    m4[e] &= nv >= 4 ? 0xFFFFFFFFu : ((1u << (8 * nv)) - 1u);
-                  }
-                }
                 uint32_t v[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -732,21 +760,37 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
       const int kt = 32 * q + lane;  // key within the tile
 #pragma unroll
       for (int c8 = 0; c8 < C::NC / 8; ++c8) {
-        uint32_t hw[4];
+        uint32_t hw[4], lw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = c8 * 8 + 2 * e;
-          const __half2 hh =
-              __floats2half2_rn(fast_exp2(fmaf(s[c], alpha, -base_s[col0 + c])),
-                                fast_exp2(fmaf(s[c + 1], alpha, -base_s[col0 + c + 1])));
+          float b0 = -base_s[col0 + c], b1 = -base_s[col0 + c + 1];
+          if constexpr (HL) {
+            b0 += kHiLoExp;
+            b1 += kHiLoExp;
+          }
+          const float e0 = fast_exp2(fmaf(s[c], alpha, b0));
+          const float e1 = fast_exp2(fmaf(s[c + 1], alpha, b1));
+          const __half2 hh = __floats2half2_rn(e0, e1);
           const float2 fl = __half22float2(hh);
-          lpart[c] += fl.x;
-          lpart[c + 1] += fl.y;
+          if constexpr (HL) {
+            // e - fl is exact in FP32; hi + lo (22 significant bits) too
+            const __half2 ll = __floats2half2_rn(e0 - fl.x, e1 - fl.y);
+            const float2 fr = __half22float2(ll);
+            lpart[c] += fl.x + fr.x;
+            lpart[c + 1] += fl.y + fr.y;
+            lw[e] = *reinterpret_cast<const uint32_t *>(&ll);
+          } else {
+            lpart[c] += fl.x;
+            lpart[c + 1] += fl.y;
+          }
           hw[e] = *reinterpret_cast<const uint32_t *>(&hh);
         }
         const int r0 = col0 + c8 * 8;
-        *reinterpret_cast<uint4 *>(gP + sw128((uint32_t)(kt * 128 + (r0 >> 3) * 16))) =
-            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        const uint32_t po = sw128((uint32_t)(kt * 128 + (r0 >> 3) * 16));
+        *reinterpret_cast<uint4 *>(gP + po) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if constexpr (HL)
+          *reinterpret_cast<uint4 *>(gP + C::PB + po) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
@@ -794,8 +838,9 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             // stored as sum p * dec(V) * 2^-8 (exact scaling): the
-            // combine kernel's convention
-            p.ws_o[(slot + c8 * 8 + e) * D + d] = __uint_as_float(r[i][e]) * 0.00390625f;
+            // combine kernel's convention; HL also removes its 2^11
+            p.ws_o[(slot + c8 * 8 + e) * D + d] =
+                __uint_as_float(r[i][e]) * (HL ? 1.9073486328125e-06f : 0.00390625f);
           }
         }
       }
@@ -838,6 +883,7 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
     float l = 0.f;
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) l += red[(cg * 4 + qq) * 32 + c];
+    if constexpr (HL) l *= 4.8828125e-04f;  // 2^-11, exact
     const int64_t slot = cta_slot() * p.rows_pad + cta_rg() * N;
     p.ws_ml[(slot + r) * 2 + 0] = m_s[r];
     p.ws_ml[(slot + r) * 2 + 1] = (aborted || bad) ? -1.f : l;
@@ -846,10 +892,10 @@ __global__ void __launch_bounds__(TcCfg<D, N>::NTHREADS, 1)
 
 // ---------------------------------------------------------------------------
 // Host side: launch of one instantiation.
-template <int D, int N, int MODE>
+template <int D, int N, int MODE, bool HL>
 cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &map,
                       cudaStream_t stream) {
-  using C = TcCfg<D, N>;
+  using C = TcCfg<D, N, HL>;
   // the shared-memory opt-in is a function attribute of the device's
   // context: set it once per context (a context made after cudaDeviceReset
   // starts without it)
@@ -860,7 +906,7 @@ cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &
   const unsigned long long ctx = current_context_id();
   if (dev < 0 || dev >= kDevs || ctx == 0 ||
       configured[dev].load(std::memory_order_acquire) != ctx) {
-    cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<D, N, MODE>,
+    cudaError_t e = cudaFuncSetAttribute(split_tc_kernel<D, N, MODE, HL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kDevs) configured[dev].store(current_context_id(), std::memory_order_release);
@@ -881,26 +927,26 @@ cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<D, N, MODE>, p, a, map);
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<D, N, MODE, HL>, p, a, map);
 }
 
 // Every (head dim, padded rows) instantiation of one plan mode.
-template <int MODE>
+template <int MODE, bool HL>
 cudaError_t launch_tc_any(const SplitParams &p, const TcArgs &a, int n, const CUtensorMap &map,
                           cudaStream_t stream) {
   switch (p.D * 1000 + n) {
-    case 64016: return launch_tc<64, 16, MODE>(p, a, map, stream);
-    case 64032: return launch_tc<64, 32, MODE>(p, a, map, stream);
-    case 64048: return launch_tc<64, 48, MODE>(p, a, map, stream);
-    case 64064: return launch_tc<64, 64, MODE>(p, a, map, stream);
-    case 128016: return launch_tc<128, 16, MODE>(p, a, map, stream);
-    case 128032: return launch_tc<128, 32, MODE>(p, a, map, stream);
-    case 128048: return launch_tc<128, 48, MODE>(p, a, map, stream);
-    case 128064: return launch_tc<128, 64, MODE>(p, a, map, stream);
-    case 256016: return launch_tc<256, 16, MODE>(p, a, map, stream);
-    case 256032: return launch_tc<256, 32, MODE>(p, a, map, stream);
-    case 256048: return launch_tc<256, 48, MODE>(p, a, map, stream);
-    case 256064: return launch_tc<256, 64, MODE>(p, a, map, stream);
+    case 64016: return launch_tc<64, 16, MODE, HL>(p, a, map, stream);
+    case 64032: return launch_tc<64, 32, MODE, HL>(p, a, map, stream);
+    case 64048: return launch_tc<64, 48, MODE, HL>(p, a, map, stream);
+    case 64064: return launch_tc<64, 64, MODE, HL>(p, a, map, stream);
+    case 128016: return launch_tc<128, 16, MODE, HL>(p, a, map, stream);
+    case 128032: return launch_tc<128, 32, MODE, HL>(p, a, map, stream);
+    case 128048: return launch_tc<128, 48, MODE, HL>(p, a, map, stream);
+    case 128064: return launch_tc<128, 64, MODE, HL>(p, a, map, stream);
+    case 256016: return launch_tc<256, 16, MODE, HL>(p, a, map, stream);
+    case 256032: return launch_tc<256, 32, MODE, HL>(p, a, map, stream);
+    case 256048: return launch_tc<256, 48, MODE, HL>(p, a, map, stream);
+    case 256064: return launch_tc<256, 64, MODE, HL>(p, a, map, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -6,7 +6,8 @@ namespace vae4 {
 
 cudaError_t launch_split_tc_dev(const SplitParams &p, const TcArgs &a, int n,
                                 const CUtensorMap &map, cudaStream_t stream) {
-  return launch_tc_any<kPlanDevice>(p, a, n, map, stream);
+  return p.hilo ? launch_tc_any<kPlanDevice, true>(p, a, n, map, stream)
+                : launch_tc_any<kPlanDevice, false>(p, a, n, map, stream);
 }
 
 }  // namespace vae4

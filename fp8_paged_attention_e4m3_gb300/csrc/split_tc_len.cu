@@ -8,7 +8,8 @@ namespace vae4 {
 
 cudaError_t launch_split_tc_len(const SplitParams &p, const TcArgs &a, int n,
                                 const CUtensorMap &map, cudaStream_t stream) {
-  return launch_tc_any<kPlanFromLen>(p, a, n, map, stream);
+  return p.hilo ? launch_tc_any<kPlanFromLen, true>(p, a, n, map, stream)
+                : launch_tc_any<kPlanFromLen, false>(p, a, n, map, stream);
 }
 
 }  // namespace vae4

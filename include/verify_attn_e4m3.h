@@ -54,7 +54,7 @@ extern "C" {
 /* ABI revision.  A wrapper refuses a library whose revision differs from the
  * one it was written for, so an out-of-date library is refused rather than
  * used (PR #524, Scope and non-duplication; PR #560, Purpose). */
-#define VAE4_ABI_VERSION 1
+#define VAE4_ABI_VERSION 2
 
 /* Same object as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st *vae4_stream;
@@ -87,7 +87,25 @@ typedef struct {
                                block_table columns * page size */
   int32_t num_sms;          /* SMs the plan targets; 0 -> current device */
   int32_t flags;            /* 0, or VAE4_FLAG_WARP_MMA / VAE4_FLAG_KV_E5M2 */
+  int32_t hilo_pv;          /* 1 -> P enters the value product as an FP16
+                               high part and an FP16 residual scaled by 2^11
+                               (see below); 0 -> one FP16 P */
 } vae4_options;
+
+/* hilo_pv: the high/residual representation of the softmax probabilities
+ * in the value product (PR #524 "[Kernel][SM70] Add opt-in E4M3 grouped
+ * attention with FP32 partials", Historical R6 purpose and evidence, Scope
+ * and non-duplication: the residual is multiplied by 2048 and its product
+ * scaled back by the exactly representable 1/2048).  With p the FP32
+ * probability, P_hi = fp16(p) and P_lo = fp16((p - P_hi) * 2^11); the
+ * partition accumulates P_hi.V + 2^-11 P_lo.V in FP32 and its running sum
+ * adds the same P_hi + 2^-11 P_lo, so P carries ~22 significant bits into
+ * the FP32 state instead of 11.  The kernel forms both parts from 2^11 p
+ * (so both products share one accumulator) and therefore raises its lazy
+ * running maximum at 2^4 instead of 2^12, which keeps 2^11 p inside FP16.
+ * It costs a second value MMA per key step and more running-maximum
+ * updates.  Only the default tcgen05 path implements it: with
+ * VAE4_FLAG_WARP_MMA the call returns VAE4_ERR_UNSUPPORTED. */
 
 /* Option flag: run the split stage on the warp-level tensor-core path
  * (mma.sync m16n8k16 with ldmatrix operands) instead of the default

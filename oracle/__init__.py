@@ -71,6 +71,12 @@ def _load():
             lib.oracle_verify_attn.argtypes = args
             lib.oracle_verify_attn_fmt.restype = ctypes.c_int
             lib.oracle_verify_attn_fmt.argtypes = args + [ctypes.c_int]
+            lib.oracle_verify_attn_strided.restype = ctypes.c_int
+            lib.oracle_verify_attn_strided.argtypes = (
+                [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 4 +
+                [ctypes.c_int] * 6 + [ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int])
             lib.oracle_bridge_fp16.restype = ctypes.c_int
             lib.oracle_bridge_fp16.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -167,6 +173,50 @@ def verify_attn(q, kv_pages, block_table, seq_len, q_len, kv_scales,
         ql.ctypes.data, sc.ctypes.data, B, Qmax, Hq, Hkv, D, page,
         n_pages, bt.shape[1], float(sm_scale), int(split_tokens), rows_ptr,
         n_rows, out.ctypes.data, int(threads), KV_FORMATS[kv_format])
+    if rc != 0:
+        raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
+    return out
+
+
+def verify_attn_strided(q, k_cache, v_cache, block_table, seq_len, q_len, kv_scales,
+                        sm_scale: float | None = None, split_tokens: int = 0, rows=None,
+                        threads: int = 0, kv_format: str = "e4m3") -> np.ndarray:
+    """Exact (FP64) verify attention over a cache given as separate K and V
+    arrays uint8 [n_pages][page][Hkv][D] -- any byte strides (views into a
+    padded buffer included; K and V with the same strides), d contiguous.
+    Other arguments and the result as verify_attn."""
+    lib = _load()
+    k, v = np.asarray(k_cache), np.asarray(v_cache)
+    if k.dtype != np.uint8 or v.dtype != np.uint8 or k.ndim != 4 or k.shape != v.shape:
+        raise ValueError("k_cache / v_cache: uint8 [n_pages][page][Hkv][D] of one shape")
+    if k.strides != v.strides or k.strides[3] != 1:
+        raise ValueError("k_cache / v_cache: equal strides, d contiguous")
+    n_pages, page, Hkv, D = k.shape
+    q64 = np.ascontiguousarray(np.asarray(q).astype(np.float64))
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_len, dtype=np.int32)
+    ql = np.ascontiguousarray(q_len, dtype=np.int32)
+    sc = np.ascontiguousarray(np.asarray(kv_scales).astype(np.float64))
+    B, Qmax, Hq, D2 = q64.shape
+    if D2 != D or bt.ndim != 2 or bt.shape[0] != B or sc.shape != (Hkv, 2):
+        raise ValueError("inconsistent shapes")
+    if sl.shape != (B,) or ql.shape != (B,):
+        raise ValueError("inconsistent shapes")
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    if rows is None:
+        out = np.zeros((B, Qmax, Hq, D), dtype=np.float64)
+        rows_ptr, n_rows = None, 0
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+        out = np.zeros((r.shape[0], D), dtype=np.float64)
+        rows_ptr, n_rows = r.ctypes.data, r.shape[0]
+        rows = r  # keep alive
+    rc = lib.oracle_verify_attn_strided(
+        q64.ctypes.data, k.ctypes.data, v.ctypes.data, k.strides[0], k.strides[1],
+        k.strides[2], bt.ctypes.data, sl.ctypes.data, ql.ctypes.data, sc.ctypes.data,
+        B, Qmax, Hq, Hkv, D, page, n_pages, bt.shape[1], float(sm_scale), int(split_tokens),
+        rows_ptr, n_rows, out.ctypes.data, int(threads), KV_FORMATS[kv_format])
     if rc != 0:
         raise OracleError(_ERRORS.get(rc, f"oracle error {rc}"))
     return out

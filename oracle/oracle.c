@@ -19,6 +19,16 @@
  *    5 exponent bits with bias 15, 2 mantissa bits, infinities at
  *    S.11111.00, NaN at S.11111.xx otherwise), largest finite value 57344.
  *
+ *  - Two cache layouts, read through one addressing rule: token j of
+ *    sequence b, KV head h is the D bytes at base + phys * page_stride +
+ *    (j % page) * token_stride + h * head_stride, phys = block_table[b][j /
+ *    page], with separate K and V bases.  The library's pool
+ *    [n_pages][2 (K,V)][Hkv][page][D] is one choice of bases and strides;
+ *    the pages' token-major cache [blocks][block_size][kv_heads][D] with
+ *    padded token strides (the [1,848,1,256] tensor with strides
+ *    [223872,264,256,1] of PR #524 "[Kernel][SM70] Add opt-in E4M3 grouped
+ *    attention with FP32 partials", AI integration review) is another.
+ *
  *  - Per-KV-head dequantisation x = dec(byte) * s_h, with separate scales for
  *    K and V (PR #560 "[Bugfix] Use FP32 state and E4M3 defaults for
  *    DFlash2", Test Plan and Results).
@@ -98,15 +108,20 @@ typedef struct {
   int64_t n_pages;
 } orc_shape;
 
-static const uint8_t *kv_row(const uint8_t *kv, const orc_shape *sh,
-                             int64_t phys, int kv_sel, int h, int slot) {
-  /* pool layout [n_pages][2 (K,V)][Hkv][page][D] */
-  int64_t idx = ((phys * 2 + kv_sel) * sh->Hkv + h) * (int64_t)sh->page + slot;
-  return kv + idx * sh->D;
+/* Where the cache's bytes live: K (sel 0) and V (sel 1) bases, strides in
+ * bytes of a page, a token slot and a KV head; d is contiguous. */
+typedef struct {
+  const uint8_t *base[2];
+  int64_t page_stride, token_stride, head_stride;
+} orc_cache;
+
+static const uint8_t *kv_row(const orc_cache *c, int64_t phys, int kv_sel, int h, int slot) {
+  return c->base[kv_sel] + phys * c->page_stride + (int64_t)slot * c->token_stride +
+         (int64_t)h * c->head_stride;
 }
 
 /* One output row: out[d] for (b, i, hq).  z is scratch of length >= L. */
-static int one_row(const double *q, const uint8_t *kv, const int32_t *bt,
+static int one_row(const double *q, const orc_cache *kv, const int32_t *bt,
                    const int32_t *seq_len, const int32_t *q_len,
                    const double *scales, const orc_shape *sh, double sm_scale,
                    int split_tokens, const double *dec, int b, int i, int hq,
@@ -129,7 +144,7 @@ static int one_row(const double *q, const uint8_t *kv, const int32_t *bt,
   for (int j = 0; j <= pos; ++j) {
     const int64_t phys = bt[(int64_t)b * sh->max_pages + j / sh->page];
     if (phys < 0 || phys >= sh->n_pages) return ORC_BAD_BLOCK;
-    const uint8_t *kr = kv_row(kv, sh, phys, 0, h, j % sh->page);
+    const uint8_t *kr = kv_row(kv, phys, 0, h, j % sh->page);
     double dot = 0.0;
     for (int d = 0; d < D; ++d) dot += qv[d] * (dec[kr[d]] * sK);
     z[j] = sm_scale * dot;
@@ -144,7 +159,7 @@ static int one_row(const double *q, const uint8_t *kv, const int32_t *bt,
     for (int j = 0; j <= pos; ++j) {
       const double w = exp(z[j] - zmax);
       const int64_t phys = bt[(int64_t)b * sh->max_pages + j / sh->page];
-      const uint8_t *vr = kv_row(kv, sh, phys, 1, h, j % sh->page);
+      const uint8_t *vr = kv_row(kv, phys, 1, h, j % sh->page);
       den += w;
       for (int d = 0; d < D; ++d) acc[d] += w * (dec[vr[d]] * sV);
     }
@@ -182,7 +197,7 @@ static int one_row(const double *q, const uint8_t *kv, const int32_t *bt,
     for (int j = j0; j <= j1; ++j) {
       const double w = exp(z[j] - mp);
       const int64_t phys = bt[(int64_t)b * sh->max_pages + j / sh->page];
-      const uint8_t *vr = kv_row(kv, sh, phys, 1, h, j % sh->page);
+      const uint8_t *vr = kv_row(kv, phys, 1, h, j % sh->page);
       lp += w;
       for (int d = 0; d < D; ++d) acc[d] += w * (dec[vr[d]] * sV);
     }
@@ -209,12 +224,11 @@ static int one_row(const double *q, const uint8_t *kv, const int32_t *bt,
  *   n_threads    OpenMP threads (0 = runtime default)
  * Returns ORC_OK or the first error code met.
  */
-int oracle_verify_attn_fmt(const double *q, const uint8_t *kv, const int32_t *block_table,
-                           const int32_t *seq_len, const int32_t *q_len,
-                           const double *scales, int B, int Qmax, int Hq, int Hkv,
-                           int D, int page, int64_t n_pages, int max_pages,
-                           double sm_scale, int split_tokens, const int32_t *rows,
-                           int64_t n_rows, double *out, int n_threads, int kv_format) {
+static int verify_rows(const double *q, const orc_cache *kv, const int32_t *block_table,
+                       const int32_t *seq_len, const int32_t *q_len, const double *scales,
+                       int B, int Qmax, int Hq, int Hkv, int D, int page, int64_t n_pages,
+                       int max_pages, double sm_scale, int split_tokens, const int32_t *rows,
+                       int64_t n_rows, double *out, int n_threads, int kv_format) {
   if (B < 0 || Qmax <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || page <= 0 ||
       max_pages <= 0 || Hq % Hkv != 0 || kv_format < 0 || kv_format > 1)
     return ORC_BAD_ARGS;
@@ -266,6 +280,50 @@ int oracle_verify_attn_fmt(const double *q, const uint8_t *kv, const int32_t *bl
     free(acc);
   }
   return status;
+}
+
+int oracle_verify_attn_fmt(const double *q, const uint8_t *kv, const int32_t *block_table,
+                           const int32_t *seq_len, const int32_t *q_len,
+                           const double *scales, int B, int Qmax, int Hq, int Hkv,
+                           int D, int page, int64_t n_pages, int max_pages,
+                           double sm_scale, int split_tokens, const int32_t *rows,
+                           int64_t n_rows, double *out, int n_threads, int kv_format) {
+  /* the pool [n_pages][2 (K,V)][Hkv][page][D] */
+  const int64_t slice = (int64_t)page * D;
+  orc_cache c;
+  c.base[0] = kv;
+  c.base[1] = kv + (int64_t)Hkv * slice;
+  c.page_stride = 2 * (int64_t)Hkv * slice;
+  c.token_stride = D;
+  c.head_stride = slice;
+  return verify_rows(q, &c, block_table, seq_len, q_len, scales, B, Qmax, Hq, Hkv, D, page,
+                     n_pages, max_pages, sm_scale, split_tokens, rows, n_rows, out, n_threads,
+                     kv_format);
+}
+
+/*
+ * The same attention over a cache given by explicit K and V bases and byte
+ * strides (page, token slot, KV head; d contiguous): any layout, e.g. the
+ * token-major [blocks][block_size][kv_heads][D] cache with a padded token
+ * stride.  Arguments otherwise as oracle_verify_attn_fmt.
+ */
+int oracle_verify_attn_strided(const double *q, const uint8_t *k_base, const uint8_t *v_base,
+                               int64_t page_stride, int64_t token_stride, int64_t head_stride,
+                               const int32_t *block_table, const int32_t *seq_len,
+                               const int32_t *q_len, const double *scales, int B, int Qmax,
+                               int Hq, int Hkv, int D, int page, int64_t n_pages, int max_pages,
+                               double sm_scale, int split_tokens, const int32_t *rows,
+                               int64_t n_rows, double *out, int n_threads, int kv_format) {
+  if (!k_base || !v_base) return ORC_BAD_ARGS;
+  orc_cache c;
+  c.base[0] = k_base;
+  c.base[1] = v_base;
+  c.page_stride = page_stride;
+  c.token_stride = token_stride;
+  c.head_stride = head_stride;
+  return verify_rows(q, &c, block_table, seq_len, q_len, scales, B, Qmax, Hq, Hkv, D, page,
+                     n_pages, max_pages, sm_scale, split_tokens, rows, n_rows, out, n_threads,
+                     kv_format);
 }
 
 /* Threads the OpenMP runtime would use by default (for the CPU baseline). */

@@ -194,6 +194,9 @@ def test_validation_options(lib):
     assert _call(lib, _args(), vae4.Options(0.0, 0, 0, 152, 9)) == -6   # short waits + mma.sync
     assert _call(lib, _args(), vae4.Options(0.0, 0, 0, 152, 16)) == -11
     assert _call(lib, _args(), vae4.Options(-1.0, 0, 0, 152, 0)) == -11
+    # the high/residual P split: 0 or 1, tcgen05 path only
+    assert _call(lib, _args(), vae4.Options(0.0, 0, 0, 152, 0, 2)) == -11
+    assert _call(lib, _args(), vae4.Options(0.0, 0, 0, 152, 1, 1)) == -6
     # capacity beyond what the block table can address
     assert _call(lib, _args(), vae4.Options(0.0, 0, 64 * 16 + 1, 152, 0)) == -3
     a = _args()

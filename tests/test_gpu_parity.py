@@ -31,7 +31,7 @@ def _gpu():
 
 
 def run_gpu(w, seq_len=None, q_len=None, partition_tokens=None, tensors=None, ws=None,
-            flags=0):
+            flags=0, hilo_pv=False):
     q, kv, bt, seq, sc = tensors or W.to_device(w, seq_len=seq_len, q_len=q_len)
     s = w.spec
     T = s.partition_tokens if partition_tokens is None else partition_tokens
@@ -39,7 +39,7 @@ def run_gpu(w, seq_len=None, q_len=None, partition_tokens=None, tensors=None, ws
     if ws is None:
         ws = vae4.alloc_workspace(s.B, s.Hq, s.Hkv, s.Qmax, s.D, w.capacity, T)
     vae4.verify(q, kv, bt, seq, sc, out, ws, partition_tokens=T, max_seq_len=w.capacity,
-                flags=flags)
+                flags=flags, hilo_pv=hilo_pv)
     torch.cuda.synchronize()
     return out.cpu().numpy(), ws
 
@@ -466,3 +466,49 @@ def test_plain_entry_point_matches_ex_with_defaults():
     assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
     compare(outs[0], oracle_full(w))
     assert vae4.read_status(ws) == 0
+
+
+# ---------------------------------------- high/residual P (hilo_pv option)
+def _cfg_workload(cfg):
+    cfg = dict(cfg)
+    if "spec" in cfg:
+        return W.generate(cfg["spec"])
+    cfg.pop("name", None)
+    return W.custom("hilo", **cfg)
+
+
+@pytest.mark.parametrize("cfg", SMALL + LARGE_PAGES + E5M2,
+                         ids=lambda c: c.get("name", str(c.get("seed"))))
+def test_parity_hilo(cfg):
+    """The high/residual split of P (PR #524, Historical R6 purpose and
+    evidence) meets the same bar on every small, large-page and E5M2 case."""
+    check_full(_cfg_workload(cfg), hilo_pv=True)
+
+
+@pytest.mark.parametrize("T", [0, 512])
+def test_hilo_lowers_the_error(T):
+    """P with ~22 significant bits instead of 11: the relative L2 error
+    against the FP64 oracle drops, and the step stays bitwise repeatable."""
+    w = W.custom("hilo_err", B=2, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[30000, 9000],
+                 q_lens=[8, 8], seed=75, outliers=True)
+    ref = oracle_full(w)
+    plain, _ = run_gpu(w, partition_tokens=T)
+    hilo, _ = run_gpu(w, partition_tokens=T, hilo_pv=True)
+    hilo2, _ = run_gpu(w, partition_tokens=T, hilo_pv=True)
+    assert np.array_equal(hilo.view(np.uint16), hilo2.view(np.uint16))
+    r_plain, _ = compare(plain, ref)
+    r_hilo, _ = compare(hilo, ref)
+    # the FP16 output rounding alone leaves about 1.5e-4 (a uniform
+    # half-ulp error); the P rounding adds on top of it without the split
+    r_round = np.linalg.norm(ref.astype(np.float16).astype(np.float64) - ref) / \
+        np.linalg.norm(ref)
+    print(f"rel-L2 plain {r_plain:.3e} hilo {r_hilo:.3e} fp16 rounding floor {r_round:.3e}")
+    assert r_hilo < r_plain
+    assert r_hilo < 1.15 * r_round
+
+
+def test_hilo_with_warp_mma_is_unsupported():
+    w = _cfg_workload(SMALL[1])
+    with pytest.raises(vae4.Vae4Error) as e:
+        run_gpu(w, flags=vae4.FLAG_WARP_MMA, hilo_pv=True)
+    assert e.value.code == -6

@@ -8,7 +8,9 @@
   prefix means, exact FP16 midpoints), invariances (page relocation, partition
   length) and the q1 / q8 tail identity.
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -279,3 +281,55 @@ def test_length_beyond_the_block_table_is_reported():
     a = oracle.verify_attn(w.q, w.kv_pages, w.block_table, sl, w.q_len, w.kv_scales)
     b = oracle.verify_attn(w.q, w.kv_pages, wide, sl, w.q_len, w.kv_scales)
     assert np.array_equal(a, b) and np.isfinite(a).all()
+
+
+# ------------------------------------------------ token-major, strided cache
+@pytest.mark.parametrize("kw,pad", [
+    (dict(B=2, Qmax=4, Hq=4, Hkv=2, D=16, seq_lens=[37, 5], q_lens=[4, 3]), 8),
+    (dict(B=1, Qmax=8, Hq=6, Hkv=1, D=32, seq_lens=[300], q_lens=[8], page=48), 8),
+    (dict(B=2, Qmax=2, Hq=2, Hkv=1, D=64, seq_lens=[70, 33], q_lens=[2, 1]), 0),
+])
+def test_token_major_strided_cache_gives_identical_bits(kw, pad):
+    """The same logical K/V in the library's pool and in the pages'
+    token-major layout with a padded token stride (PR #524, AI integration
+    review): the oracle reads the same bytes, so the outputs are identical
+    bit for bit, in direct and in split mode.  Padding holds NaN codes, so a
+    read of it would show."""
+    w = _small(**kw)
+    c = W.token_major(w, token_pad=pad, page_pad=16)
+    k, v = c.views()
+    assert k.strides[1] == w.spec.Hkv * w.spec.D + pad
+    for T in (0, 16):
+        a = _run(w, split_tokens=T)
+        b = oracle.verify_attn_strided(w.q, k, v, w.block_table, w.seq_len, w.q_len,
+                                       w.kv_scales, sm_scale=w.sm_scale, split_tokens=T)
+        assert np.array_equal(a, b) and np.isfinite(b).all()
+
+
+def test_token_major_counterexample_layout():
+    """The pages' counterexample view: block size 848, one KV head, D = 256,
+    strides [223872, 264, 256, 1].  The oracle over that layout matches torch
+    SDPA (float64) on the K/V gathered from it with NumPy indexing."""
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_sizes.json")))
+    ce = g["stride_counterexample"]
+    w = _small(B=1, Qmax=8, Hq=6, Hkv=1, D=256, seq_lens=[1000], q_lens=[8], page=848, seed=31)
+    c = W.token_major(w, token_pad=ce["strides"][1] - 256)
+    k, v = c.views()
+    assert list(k.strides) == ce["strides"] and list(k.shape[1:]) == ce["shape"][1:]
+    got = oracle.verify_attn_strided(w.q, k, v, w.block_table, w.seq_len, w.q_len,
+                                     w.kv_scales, sm_scale=w.sm_scale)
+    # independent reference: gather the logical K/V rows with NumPy, decode
+    # with torch's FP8 cast, attend with torch SDPA in float64
+    L, ql = int(w.seq_len[0]), int(w.q_len[0])
+    pages = w.block_table[0, np.arange(L) // 848]
+    slots = np.arange(L) % 848
+    kk = torch.from_numpy(np.ascontiguousarray(k[pages, slots, 0])).view(
+        torch.float8_e4m3fn).to(torch.float64) * float(w.kv_scales[0, 0])
+    vv = torch.from_numpy(np.ascontiguousarray(v[pages, slots, 0])).view(
+        torch.float8_e4m3fn).to(torch.float64) * float(w.kv_scales[0, 1])
+    qq = torch.from_numpy(w.q[0, :ql].astype(np.float64)).permute(1, 0, 2)  # [Hq][ql][D]
+    mask = torch.arange(L)[None, :] <= (torch.arange(ql)[:, None] + L - ql)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qq, kk[None].expand(6, -1, -1), vv[None].expand(6, -1, -1), attn_mask=mask,
+        scale=w.sm_scale).permute(1, 0, 2).numpy()
+    assert np.allclose(got[0, :ql], ref, rtol=1e-12, atol=1e-14)

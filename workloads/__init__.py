@@ -359,6 +359,54 @@ def relocate(w: Workload, seed: int) -> Workload:
     return dataclasses.replace(w, kv_pages=kv, block_table=bt.astype(np.int32))
 
 
+PAD_BYTE = 0x7F  # an E4M3 NaN code: padding that is read would show up as NaN
+
+
+@dataclasses.dataclass
+class TokenMajorCache:
+    """The workload's cache in the token-major layout of the pages:
+    separate K and V caches [n_pages][page][Hkv][D] (page = the block size),
+    token stride Hkv * D + token_pad bytes, head stride D, page stride
+    page * token stride + page_pad; d contiguous.  Padding bytes hold
+    PAD_BYTE.  K and V live in buffers of their own."""
+    k_buf: np.ndarray
+    v_buf: np.ndarray
+    shape: tuple    # (n_pages, page, Hkv, D)
+    strides: tuple  # bytes (page, token, head, 1)
+
+    def views(self):
+        """(K, V) as numpy strided views into the buffers."""
+        st = np.lib.stride_tricks.as_strided
+        return (st(self.k_buf, self.shape, self.strides, writeable=False),
+                st(self.v_buf, self.shape, self.strides, writeable=False))
+
+    def to_device(self, device="cuda"):
+        """(K, V) as torch strided views into device copies of the buffers."""
+        import torch
+        out = []
+        for buf in (self.k_buf, self.v_buf):
+            d = torch.from_numpy(buf).to(device)
+            out.append(torch.as_strided(d, self.shape, self.strides, 0))
+        return tuple(out)
+
+
+def token_major(w: Workload, token_pad: int = 0, page_pad: int = 0) -> TokenMajorCache:
+    """The same logical K/V bytes as w.kv_pages, laid out token-major with a
+    padded token stride (e.g. the pages' [1,848,1,256] block with a 264-byte
+    token stride: token_pad = 8)."""
+    n_pages, _, Hkv, page, D = w.kv_pages.shape
+    tok = Hkv * D + token_pad
+    pst = page * tok + page_pad
+    shape, strides = (n_pages, page, Hkv, D), (pst, tok, D, 1)
+    bufs = []
+    for sel in range(2):
+        buf = np.full(n_pages * pst, PAD_BYTE, dtype=np.uint8)
+        view = np.lib.stride_tricks.as_strided(buf, shape, strides)
+        view[...] = w.kv_pages[:, sel].transpose(0, 2, 1, 3)  # [n][Hkv][page][D] -> [n][page][Hkv][D]
+        bufs.append(buf)
+    return TokenMajorCache(bufs[0], bufs[1], shape, strides)
+
+
 def to_device(w: Workload, device="cuda", seq_len=None, q_len=None):
     """The workload's inputs as device tensors for the library:
     (q, kv_pages, block_table, seq_lens [B][2] = (L, q_len), kv_scales)."""
