@@ -42,7 +42,7 @@ EXPORTS = (
     "verify_attn_e4m3_strerror", "verify_attn_e4m3_read_status",
     "verify_attn_e4m3_clear_status", "verify_attn_e4m3_decode_table",
     "verify_attn_e4m3_noalloc", "verify_attn_e4m3_kv_read",
-    "verify_attn_e4m3_bridge_fp16",
+    "verify_attn_e4m3_bridge_fp16", "verify_attn_e4m3_kv",
 )
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -99,6 +99,8 @@ def load(build_if_stale: bool = True):
                      "verify_attn_e4m3_combine", "verify_attn_e4m3_kv_read"):
             getattr(lib, name).argtypes = [P] * 7 + [ctypes.c_void_p, ctypes.POINTER(Options)]
             getattr(lib, name).restype = ctypes.c_int
+        lib.verify_attn_e4m3_kv.argtypes = [P] * 8 + [ctypes.c_void_p, ctypes.POINTER(Options)]
+        lib.verify_attn_e4m3_kv.restype = ctypes.c_int
         lib.verify_attn_e4m3_bridge_fp16.argtypes = [P] * 6 + [ctypes.c_void_p, ctypes.c_int32,
                                                                ctypes.c_void_p]
         lib.verify_attn_e4m3_bridge_fp16.restype = ctypes.c_int
@@ -204,6 +206,25 @@ def verify_attn_e4m3(q, kv_pages, block_table, seq_lens, kv_scales, out, workspa
 
 
 verify = verify_attn_e4m3
+
+
+def verify_attn_e4m3_kv(q, k_cache, v_cache, block_table, seq_lens, kv_scales, out, workspace,
+                        *, softmax_scale: float = 0.0, partition_tokens: int = 0,
+                        max_seq_len: int = 0, num_sms: int = 0, flags: int = 0,
+                        hilo_pv: bool = False, stream=None):
+    """The verify step over separate K and V caches uint8 [n_pages][page]
+    [Hkv][D] in any strided layout (token-major, padded token strides that
+    are multiples of 8 bytes); see the header.  Other arguments as
+    verify_attn_e4m3."""
+    lib = load()
+    opt = Options(float(softmax_scale), int(partition_tokens), int(max_seq_len),
+                  int(num_sms), int(flags), int(bool(hilo_pv)))
+    descs = [describe(t) for t in (q, k_cache, v_cache, block_table, seq_lens, kv_scales,
+                                   out, workspace)]
+    rc = lib.verify_attn_e4m3_kv(*[ctypes.byref(x) for x in descs],
+                                 ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(opt))
+    _check(rc, "verify_attn_e4m3_kv")
+    return out
 
 
 def _stage(name, q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, *,

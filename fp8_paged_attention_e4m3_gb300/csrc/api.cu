@@ -144,6 +144,75 @@ int check_qo(const vae4_tensor *t) {
   return VAE4_OK;
 }
 
+// A validated KV cache: the pool form (one tensor, the mma.sync kernel and
+// the gather floor read it too) or separate K and V caches with strides.
+struct KvSrc {
+  const uint8_t *pool;  // pool form, else null
+  const uint8_t *kb, *vb;
+  int64_t k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;  // bytes
+  int64_t n_pages, Hkv, page;
+};
+
+// kv pages: U8 [n_pages][2][Hkv][page][D], contiguous
+int check_pool(const vae4_tensor *kv, int64_t D, KvSrc *o) {
+  if (kv->dtype != VAE4_U8) return VAE4_ERR_DTYPE;
+  if (kv->ndim != 5 || kv->shape[1] != 2 || kv->shape[4] != D || kv->shape[0] < 1 ||
+      kv->shape[2] < 1)
+    return VAE4_ERR_SHAPE;
+  const int64_t n_pages = kv->shape[0], Hkv = kv->shape[2], page = kv->shape[3];
+  // any multiple of 16 tokens: the kernels move 16-key page slices
+  if (page < 16 || page % 16 != 0 || page > 65536) return VAE4_ERR_UNSUPPORTED;
+  if (kv->stride[4] != 1 || kv->stride[3] != D || kv->stride[2] != page * D ||
+      kv->stride[1] != Hkv * page * D || kv->stride[0] != 2 * Hkv * page * D)
+    return VAE4_ERR_STRIDE;
+  if (!al16(kv->data)) return VAE4_ERR_MISALIGNED;
+  if (n_pages * 2 * Hkv * page > (int64_t)0x7fffff00) return VAE4_ERR_SHAPE;
+  const uint8_t *b = static_cast<const uint8_t *>(kv->data);
+  o->pool = b;
+  o->kb = b;
+  o->vb = b ? b + Hkv * page * D : nullptr;
+  o->k_ps = o->v_ps = 2 * Hkv * page * D;
+  o->k_ts = o->v_ts = D;
+  o->k_hs = o->v_hs = page * D;
+  o->n_pages = n_pages;
+  o->Hkv = Hkv;
+  o->page = page;
+  return VAE4_OK;
+}
+
+// separate caches: U8 [n_pages][page][Hkv][D] each, same shape, d
+// contiguous, other strides any multiples of 8 bytes, bases 8-byte aligned
+int check_kv(const vae4_tensor *k, const vae4_tensor *v, int64_t D, KvSrc *o) {
+  for (const vae4_tensor *t : {k, v}) {
+    if (t->dtype != VAE4_U8) return VAE4_ERR_DTYPE;
+    if (t->ndim != 4 || t->shape[3] != D || t->shape[0] < 1 || t->shape[2] < 1)
+      return VAE4_ERR_SHAPE;
+    for (int d = 0; d < 4; ++d)
+      if (t->shape[d] != k->shape[d]) return VAE4_ERR_SHAPE;
+    if (t->stride[3] != 1) return VAE4_ERR_STRIDE;
+    for (int d = 0; d < 3; ++d)
+      if (t->stride[d] < 0 || t->stride[d] % 8 != 0 || t->stride[d] >= ((int64_t)1 << 40))
+        return VAE4_ERR_STRIDE;
+    if ((reinterpret_cast<uintptr_t>(t->data) & 7u) != 0) return VAE4_ERR_MISALIGNED;
+  }
+  const int64_t page = k->shape[1];
+  if (page < 16 || page % 16 != 0 || page > 65536) return VAE4_ERR_UNSUPPORTED;
+  if (k->shape[0] > 0x7fffffff) return VAE4_ERR_SHAPE;
+  o->pool = nullptr;
+  o->kb = static_cast<const uint8_t *>(k->data);
+  o->vb = static_cast<const uint8_t *>(v->data);
+  o->k_ps = k->stride[0];
+  o->k_ts = k->stride[1];
+  o->k_hs = k->stride[2];
+  o->v_ps = v->stride[0];
+  o->v_ts = v->stride[1];
+  o->v_hs = v->stride[2];
+  o->n_pages = k->shape[0];
+  o->Hkv = k->shape[2];
+  o->page = page;
+  return VAE4_OK;
+}
+
 struct Prepared {
   SplitParams sp;
   CombineParams cp;
@@ -166,10 +235,12 @@ cudaError_t launch_split(const Prepared &pr, cudaStream_t st) {
                      : vae4::launch_split_tc(pr.sp, pr.wait_limit, st);
 }
 
-int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
-            const vae4_tensor *seq, const vae4_tensor *sc, const vae4_tensor *out,
-            const vae4_tensor *ws, const vae4_options *opt, Prepared *pr) {
-  if (!q || !kv || !bt || !seq || !sc || !out || !ws) return VAE4_ERR_NULL;
+// kv: the pool; or k and v (kv == null): separate caches
+int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *kc,
+            const vae4_tensor *vc, const vae4_tensor *bt, const vae4_tensor *seq,
+            const vae4_tensor *sc, const vae4_tensor *out, const vae4_tensor *ws,
+            const vae4_options *opt, Prepared *pr) {
+  if (!q || !(kv || (kc && vc)) || !bt || !seq || !sc || !out || !ws) return VAE4_ERR_NULL;
   vae4_options o;
   memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
@@ -177,7 +248,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
     return VAE4_ERR_OPTIONS;
   if (o.hilo_pv != 0 && o.hilo_pv != 1) return VAE4_ERR_OPTIONS;
   if ((o.flags & VAE4_FLAG_WARP_MMA) &&
-      ((o.flags & (VAE4_FLAG_KV_E5M2 | VAE4_FLAG_TEST_SHORT_WAITS)) || o.hilo_pv))
+      ((o.flags & (VAE4_FLAG_KV_E5M2 | VAE4_FLAG_TEST_SHORT_WAITS)) || o.hilo_pv || !kv))
     return VAE4_ERR_UNSUPPORTED;
 
   int rc = check_qo(q);
@@ -190,20 +261,10 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   if (D != 64 && D != 128 && D != 256) return VAE4_ERR_UNSUPPORTED;
   if (Qmax < 1 || Qmax > kMaxQmax || Hq < 1 || B > 65535) return VAE4_ERR_SHAPE;
 
-  // kv pages: U8 [n_pages][2][Hkv][page][D], contiguous
-  if (kv->dtype != VAE4_U8) return VAE4_ERR_DTYPE;
-  if (kv->ndim != 5 || kv->shape[1] != 2 || kv->shape[4] != D || kv->shape[0] < 1 ||
-      kv->shape[2] < 1)
-    return VAE4_ERR_SHAPE;
-  const int64_t n_pages = kv->shape[0], Hkv = kv->shape[2], page = kv->shape[3];
-  // any multiple of 16 tokens: the kernels move 16-key page slices
-  if (page < 16 || page % 16 != 0 || page > 65536) return VAE4_ERR_UNSUPPORTED;
-  if (kv->stride[4] != 1 || kv->stride[3] != D || kv->stride[2] != page * D ||
-      kv->stride[1] != Hkv * page * D || kv->stride[0] != 2 * Hkv * page * D)
-    return VAE4_ERR_STRIDE;
-  if (!al16(kv->data)) return VAE4_ERR_MISALIGNED;
-  // the pool is addressed as rows of D bytes by 32-bit TMA coordinates
-  if (n_pages * 2 * Hkv * page > (int64_t)0x7fffff00) return VAE4_ERR_SHAPE;
+  KvSrc src;
+  rc = kv ? check_pool(kv, D, &src) : check_kv(kc, vc, D, &src);
+  if (rc) return rc;
+  const int64_t n_pages = src.n_pages, Hkv = src.Hkv, page = src.page;
   if (Hq % Hkv != 0) return VAE4_ERR_GQA;
   const int64_t G = Hq / Hkv;
   const int64_t rows = Qmax * G;
@@ -273,7 +334,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   pr->wait_limit = (o.flags & VAE4_FLAG_TEST_SHORT_WAITS) ? kShortWaitCycles : kWaitLimitCycles;
   pr->num_sms = sms;
   if (B > 0 && ws->shape[0] < lay.total) return VAE4_ERR_WORKSPACE;
-  if (!q->data || !kv->data || !bt->data || !seq->data || !sc->data || !out->data ||
+  if (!q->data || !src.kb || !src.vb || !bt->data || !seq->data || !sc->data || !out->data ||
       !ws->data) {
     if (B > 0) return VAE4_ERR_NULL;
   }
@@ -291,8 +352,16 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *bt,
   s.q_sb = q->stride[0];
   s.q_si = q->stride[1];
   s.q_sh = q->stride[2];
-  s.kv = static_cast<const uint8_t *>(kv->data);
+  s.kv = src.pool;
   s.n_pages = n_pages;
+  s.k_base = src.kb;
+  s.v_base = src.vb;
+  s.k_ps = src.k_ps;
+  s.k_ts = src.k_ts;
+  s.k_hs = src.k_hs;
+  s.v_ps = src.v_ps;
+  s.v_ts = src.v_ts;
+  s.v_hs = src.v_hs;
   s.bt = static_cast<const int32_t *>(bt->data);
   s.bt_sb = bt->stride[0];
   s.max_pages = (int32_t)max_pages;
@@ -467,7 +536,24 @@ int verify_attn_e4m3_ex(const vae4_tensor *q, const vae4_tensor *kv_pages,
                         const vae4_tensor *workspace, vae4_stream stream,
                         const vae4_options *opt) {
   Prepared pr;
-  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  int rc = prepare(q, kv_pages, nullptr, nullptr, block_table, seq_lens, kv_scales, out,
+                   workspace, opt, &pr);
+  if (rc) return rc;
+  if (pr.empty) return VAE4_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_split(pr, st) != cudaSuccess) return VAE4_ERR_CUDA;
+  if (vae4::launch_combine(pr.cp, st) != cudaSuccess) return VAE4_ERR_CUDA;
+  return VAE4_OK;
+}
+
+int verify_attn_e4m3_kv(const vae4_tensor *q, const vae4_tensor *k_cache,
+                        const vae4_tensor *v_cache, const vae4_tensor *block_table,
+                        const vae4_tensor *seq_lens, const vae4_tensor *kv_scales,
+                        const vae4_tensor *out, const vae4_tensor *workspace,
+                        vae4_stream stream, const vae4_options *opt) {
+  Prepared pr;
+  int rc = prepare(q, nullptr, k_cache, v_cache, block_table, seq_lens, kv_scales, out, workspace,
+                   opt, &pr);
   if (rc) return rc;
   if (pr.empty) return VAE4_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -482,7 +568,8 @@ int verify_attn_e4m3_partials(const vae4_tensor *q, const vae4_tensor *kv_pages,
                               const vae4_tensor *workspace, vae4_stream stream,
                               const vae4_options *opt) {
   Prepared pr;
-  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  int rc = prepare(q, kv_pages, nullptr, nullptr, block_table, seq_lens, kv_scales, out,
+                   workspace, opt, &pr);
   if (rc) return rc;
   if (pr.empty) return VAE4_OK;
   if (launch_split(pr, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -496,7 +583,8 @@ int verify_attn_e4m3_combine(const vae4_tensor *q, const vae4_tensor *kv_pages,
                              const vae4_tensor *workspace, vae4_stream stream,
                              const vae4_options *opt) {
   Prepared pr;
-  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  int rc = prepare(q, kv_pages, nullptr, nullptr, block_table, seq_lens, kv_scales, out,
+                   workspace, opt, &pr);
   if (rc) return rc;
   if (pr.empty) return VAE4_OK;
   if (vae4::launch_combine(pr.cp, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -510,7 +598,8 @@ int verify_attn_e4m3_kv_read(const vae4_tensor *q, const vae4_tensor *kv_pages,
                              const vae4_tensor *workspace, vae4_stream stream,
                              const vae4_options *opt) {
   Prepared pr;
-  int rc = prepare(q, kv_pages, block_table, seq_lens, kv_scales, out, workspace, opt, &pr);
+  int rc = prepare(q, kv_pages, nullptr, nullptr, block_table, seq_lens, kv_scales, out,
+                   workspace, opt, &pr);
   if (rc) return rc;
   if (pr.empty) return VAE4_OK;
   if (vae4::launch_kv_read(pr.sp, pr.num_sms, reinterpret_cast<cudaStream_t>(stream)) !=

@@ -14,8 +14,14 @@ constexpr int kDevPlanMaxB = 1024;
 struct SplitParams {
   const void *q;        // fp16 [B][Qmax][Hq][D]
   int64_t q_sb, q_si, q_sh;
-  const uint8_t *kv;    // u8 [n_pages][2][Hkv][page][D]
+  const uint8_t *kv;    // u8 [n_pages][2][Hkv][page][D] (the pool form; null for separate K/V)
   int64_t n_pages;
+  // Where token t of KV head h in physical page ph lives, for K and for V:
+  // base + ph * ps + (t % page) * ts + h * hs (bytes; d contiguous).  The
+  // pool form is one choice of these; the token-major cache another.
+  const uint8_t *k_base, *v_base;
+  int64_t k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;
+  int32_t kv_cpasync;   // 1: strides are multiples of 8 but not all of 16 (8-byte copies)
   const int32_t *bt;    // i32 [B][max_pages]
   int64_t bt_sb;
   int32_t max_pages;
@@ -65,8 +71,14 @@ struct CombineParams {
 
 // The bridge kernel's parameters (paged FP8 -> dense FP16 K and V).
 struct BridgeParams {
-  const uint8_t *kv;    // u8 [n_pages][2][Hkv][page][D]
+  const uint8_t *kv;    // u8 [n_pages][2][Hkv][page][D] (the pool form; null for separate K/V)
   int64_t n_pages;
+  // Where token t of KV head h in physical page ph lives, for K and for V:
+  // base + ph * ps + (t % page) * ts + h * hs (bytes; d contiguous).  The
+  // pool form is one choice of these; the token-major cache another.
+  const uint8_t *k_base, *v_base;
+  int64_t k_ps, k_ts, k_hs, v_ps, v_ts, v_hs;
+  int32_t kv_cpasync;   // 1: strides are multiples of 8 but not all of 16 (8-byte copies)
   const int32_t *bt;    // i32 [B][max_pages]
   int64_t bt_sb;
   const int32_t *seq;   // i32 [B] or [B][2] (L first)

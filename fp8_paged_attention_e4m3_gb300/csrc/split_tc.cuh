@@ -68,7 +68,6 @@
 namespace vae4 {
 
 struct TcArgs {
-  int64_t rows_total;    // rows of D bytes in the pool view of the tensor map
   long long wait_limit;   // SM cycles before a pipeline wait gives up
   long long drain_limit;  // SM cycles the wind-down waits for copies and MMAs in flight
   int32_t n_rg;          // row groups per KV head
@@ -162,6 +161,88 @@ static __device__ __noinline__ void zero_v_tail(uint8_t *raw, int kz, int dq, in
   __syncwarp();
 }
 
+// Producer of one ring (K or V) for caches whose strides are multiples of 8
+// bytes but not all of 16 (the pages' 264-byte token stride, PR #524
+// "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32 partials", AI
+// integration review), which no tensor map can describe: every key row of a
+// half-tile arrives as 8-byte asynchronous copies into the same swizzled
+// slot layout the tensor loads produce, and each lane's completion arrives
+// on the slot's "full" barrier (32 arrivals per phase).  Keys past the
+// partition and pages with invalid ids are zero-filled.  Out of line: the
+// tensor-load producer is the hot path.  Returns the half-tiles issued.
+template <int D>
+static __device__ __noinline__ int cpa_produce(const SplitParams &p, int h, int k0, int k1,
+                                               int nhalf, bool isv, uint32_t ring, uint32_t full0,
+                                               uint32_t empty0, int nslot, volatile int *abort_f,
+                                               long long lim, volatile int *bad_f, int cur,
+                                               int nxt, int lp_base, const int32_t *btb,
+                                               int lane) {
+  constexpr int IB = D < 128 ? D : 128, SMASK = IB == 128 ? 7 : 3;
+  constexpr int CPK = D / 8, KPI = 32 / CPK;  // 8-byte chunks per key, keys per instruction
+  constexpr int RSLOT = 64 * D;
+  const uint8_t *hbase = (isv ? p.v_base : p.k_base) + (int64_t)h * (isv ? p.v_hs : p.k_hs);
+  const int64_t ps = isv ? p.v_ps : p.k_ps, ts = isv ? p.v_ts : p.k_ts;
+  const uint64_t pol = tc::l2_evict_first_policy();
+  const int c = lane % CPK, kk = lane / CPK;
+  const int dh = (8 * c) / IB, cb = (8 * c) % IB;  // this lane's chunk: IB block, byte in it
+  const int ppb = p.page >> 4;
+  const int box0 = (k0 >> 4) + lane;  // lane g < 4: box g of the first half-tile
+  int lpg = box0 / ppb, sbg = box0 - lpg * ppb;
+  int st = 0, u = 0, n_issued = 0;
+  for (int t = 0; t < nhalf; ++t) {
+    if (u > 0 && !tc::mbar_wait(empty0 + 8u * st, (u - 1) & 1, abort_f, lim)) break;
+    n_issued = t + 1;
+    const int rel = lpg - lp_base;
+    const int pc = __shfl_sync(0xffffffffu, cur, rel & 31);
+    const int pn = __shfl_sync(0xffffffffu, nxt, rel & 31);
+    int phys = -1;  // lanes 0-3: page of box `lane`, -1 = zero fill
+    if (lane < 4 && k0 + 64 * t + 16 * lane < k1) {
+      const int ph = rel < 32 ? pc : pn;
+      if (ph >= 0 && ph < p.n_pages)
+        phys = ph;
+      else
+        *bad_f = 1;
+    }
+    const uint32_t slot = ring + st * RSLOT;
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      const int pg = __shfl_sync(0xffffffffu, phys, g);
+      const int sb = __shfl_sync(0xffffffffu, sbg, g);
+      const int key0 = k0 + 64 * t + 16 * g;  // first key of box g
+      const uint8_t *src = hbase + (int64_t)max(pg, 0) * ps + (int64_t)(16 * sb + kk) * ts + 8 * c;
+#pragma unroll
+      for (int r = kk; r < 16; r += KPI) {
+        const bool ok = pg >= 0 && key0 + r < k1;
+        const uint32_t off = (uint32_t)(r * IB + cb);
+        tc::cp_async8_hint(slot + g * (16 * D) + dh * (16 * IB) + (off ^ (((off >> 7) & SMASK) << 4)),
+                           ok ? src : hbase, ok ? 8 : 0, pol);
+        src += KPI * ts;
+      }
+    }
+    tc::cp_async_mbar_arrive_noinc(full0 + 8u * st);
+    if (ppb == 1) {
+      lpg += 4;
+    } else {
+      sbg += 4;
+      while (sbg >= ppb) {
+        sbg -= ppb;
+        ++lpg;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, lpg, 0) >= lp_base + 32) {  // slide the window
+      cur = nxt;
+      lp_base += 32;
+      const int lp = lp_base + 32 + lane;
+      nxt = lp < p.max_pages ? __ldg(btb + lp) : -1;
+    }
+    if (++st == nslot) {
+      st = 0;
+      ++u;
+    }
+  }
+  return n_issued;
+}
+
 // Partition plans, one instantiation each so none carries another's code:
 // kPlanFixed: static grid (partition, head x row group, sequence), T given;
 // kPlanFromLen: static grid, T from each sequence's length (the automatic
@@ -170,7 +251,8 @@ static __device__ __noinline__ void zero_v_tail(uint8_t *raw, int kz, int dq, in
 enum { kPlanFixed = 0, kPlanFromLen = 1, kPlanDevice = 2 };
 template <int D, int N, int MODE, bool HL>
 __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
-    split_tc_kernel(const SplitParams p, const TcArgs a, const __grid_constant__ CUtensorMap tmap) {
+    split_tc_kernel(const SplitParams p, const TcArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v) {
   using C = TcCfg<D, N, HL>;
   constexpr int kKFull = C::B_KFULL, kKEmpty = C::B_KEMPTY, kVFull = C::B_VFULL,
                 kVEmpty = C::B_VEMPTY, kKReady = C::B_KREADY, kKFree = C::B_KFREE,
@@ -234,12 +316,16 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
         cnt = 128;
       else if ((i >= kSFree && i < kSFree + 2) || i == kPReady)
         cnt = 32 * C::NSW;
+      else if (p.kv_cpasync && ((i >= kKFull && i < kKFull + C::NKR) ||
+                                (i >= kVFull && i < kVFull + C::NVR)))
+        cnt = 32;  // one arrival per producer lane (8-byte copies)
       tc::mbar_init(bar(i), cnt);
     }
     *abort_f = 0;
     *bad_f = 0;
   }
-  if (producer && lane == 0) tc::prefetch_tensormap(&tmap);  // a kernel parameter
+  if (producer && lane == 0 && !p.kv_cpasync)  // kernel parameters
+    tc::prefetch_tensormap(warp == kWVProd ? &tmap_v : &tmap_k);
   if (warp == kWQk) {
     tc::tmem_alloc(sSm + kSmTslot, 512);
     tc::tmem_relinquish();
@@ -422,9 +508,12 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
     const int ppb = p.page >> 4;        // 16-key boxes per page
     const int box0 = (k0 >> 4) + lane;  // lane g < 4: box g of the first half-tile
     int lpg = box0 / ppb, sbg = box0 - lpg * ppb;
-    const int rowhead = (isv ? p.Hkv : 0) + h;  // row = (phys * 2Hkv + rowhead) * page + 16 sb
+    const CUtensorMap *map = isv ? &tmap_v : &tmap_k;
     int st = 0, u = 0;  // ring slot and pass of half-tile t (t = u * nslot + st)
-    for (int t = 0; t < nhalf; ++t) {
+    if (p.kv_cpasync)
+      n_issued = cpa_produce<D>(p, h, k0, k1, nhalf, isv, ring, bar(fullb), bar(emptyb), nslot,
+                                abort_f, LIM, bad_f, cur, nxt, lp_base, btb, lane);
+    for (int t = 0; t < (p.kv_cpasync ? 0 : nhalf); ++t) {
       if (u > 0 && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
       if (lane == 0) tc::mbar_arrive_expect_tx(bar(fullb + st), C::RSLOT);
       n_issued = t + 1;
@@ -435,15 +524,16 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
       const int pn = __shfl_sync(0xffffffffu, nxt, rel & 31);
       if (lane < 4) {
         const int phys = rel < 32 ? pc : pn;
-        int row = (int)a.rows_total;  // outside the tensor: zero fill
+        int pgc = (int)p.n_pages;  // outside the tensor: zero fill
         if (k0 + 64 * t + 16 * lane < k1) {
           if (phys >= 0 && phys < p.n_pages)
-            row = (phys * (2 * p.Hkv) + rowhead) * p.page + 16 * sbg;  // < 2^31 (checked)
+            pgc = phys;
           else
             *bad_f = 1;
         }
-        // one box: 16 keys x D bytes, as NDH blocks of 16 x IB (swizzled)
-        tc::tma_load_3d_hint(ring + st * C::RSLOT + lane * (16 * D), &tmap, 0, row, 0,
+        // one box: 16 keys x D bytes of head h, as NDH blocks of 16 x IB
+        // (swizzled); coordinates (byte, token in page, block, head, page)
+        tc::tma_load_5d_hint(ring + st * C::RSLOT + lane * (16 * D), map, 0, 16 * sbg, 0, h, pgc,
                              bar(fullb + st), pol);
       }
       if (ppb == 1) {
@@ -863,6 +953,7 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
       tc::mbar_wait(bar(fullb + s), (uses - 1) & 1, &no_abort, a.drain_limit);
     }
   }
+  if (producer && p.kv_cpasync) tc::cp_async_wait_all();  // every lane's own copies
   if (drain && (warp == kWQk || warp == kWPv) && lane == 0 && mma_issued) {
     const uint32_t db = bar(warp == kWQk ? kDrainQk : kDrainPv);
     tc::mma_commit(db);
@@ -893,8 +984,8 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
 // ---------------------------------------------------------------------------
 // Host side: launch of one instantiation.
 template <int D, int N, int MODE, bool HL>
-cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &map,
-                      cudaStream_t stream) {
+cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &map_k,
+                      const CUtensorMap &map_v, cudaStream_t stream) {
   using C = TcCfg<D, N, HL>;
   // the shared-memory opt-in is a function attribute of the device's
   // context: set it once per context (a context made after cudaDeviceReset
@@ -927,26 +1018,26 @@ cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_tc_kernel<D, N, MODE, HL>, p, a, map);
+  return cudaLaunchKernelEx(&cfg, split_tc_kernel<D, N, MODE, HL>, p, a, map_k, map_v);
 }
 
 // Every (head dim, padded rows) instantiation of one plan mode.
 template <int MODE, bool HL>
-cudaError_t launch_tc_any(const SplitParams &p, const TcArgs &a, int n, const CUtensorMap &map,
-                          cudaStream_t stream) {
+cudaError_t launch_tc_any(const SplitParams &p, const TcArgs &a, int n, const CUtensorMap &map_k,
+                          const CUtensorMap &map_v, cudaStream_t stream) {
   switch (p.D * 1000 + n) {
-    case 64016: return launch_tc<64, 16, MODE, HL>(p, a, map, stream);
-    case 64032: return launch_tc<64, 32, MODE, HL>(p, a, map, stream);
-    case 64048: return launch_tc<64, 48, MODE, HL>(p, a, map, stream);
-    case 64064: return launch_tc<64, 64, MODE, HL>(p, a, map, stream);
-    case 128016: return launch_tc<128, 16, MODE, HL>(p, a, map, stream);
-    case 128032: return launch_tc<128, 32, MODE, HL>(p, a, map, stream);
-    case 128048: return launch_tc<128, 48, MODE, HL>(p, a, map, stream);
-    case 128064: return launch_tc<128, 64, MODE, HL>(p, a, map, stream);
-    case 256016: return launch_tc<256, 16, MODE, HL>(p, a, map, stream);
-    case 256032: return launch_tc<256, 32, MODE, HL>(p, a, map, stream);
-    case 256048: return launch_tc<256, 48, MODE, HL>(p, a, map, stream);
-    case 256064: return launch_tc<256, 64, MODE, HL>(p, a, map, stream);
+    case 64016: return launch_tc<64, 16, MODE, HL>(p, a, map_k, map_v, stream);
+    case 64032: return launch_tc<64, 32, MODE, HL>(p, a, map_k, map_v, stream);
+    case 64048: return launch_tc<64, 48, MODE, HL>(p, a, map_k, map_v, stream);
+    case 64064: return launch_tc<64, 64, MODE, HL>(p, a, map_k, map_v, stream);
+    case 128016: return launch_tc<128, 16, MODE, HL>(p, a, map_k, map_v, stream);
+    case 128032: return launch_tc<128, 32, MODE, HL>(p, a, map_k, map_v, stream);
+    case 128048: return launch_tc<128, 48, MODE, HL>(p, a, map_k, map_v, stream);
+    case 128064: return launch_tc<128, 64, MODE, HL>(p, a, map_k, map_v, stream);
+    case 256016: return launch_tc<256, 16, MODE, HL>(p, a, map_k, map_v, stream);
+    case 256032: return launch_tc<256, 32, MODE, HL>(p, a, map_k, map_v, stream);
+    case 256048: return launch_tc<256, 48, MODE, HL>(p, a, map_k, map_v, stream);
+    case 256064: return launch_tc<256, 64, MODE, HL>(p, a, map_k, map_v, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -954,8 +1045,10 @@ cudaError_t launch_tc_any(const SplitParams &p, const TcArgs &a, int n, const CU
 // The other plan modes' instantiations, each compiled in a translation unit
 // of its own.
 cudaError_t launch_split_tc_dev(const SplitParams &p, const TcArgs &a, int n,
-                                const CUtensorMap &map, cudaStream_t stream);
+                                const CUtensorMap &map_k, const CUtensorMap &map_v,
+                                cudaStream_t stream);
 cudaError_t launch_split_tc_len(const SplitParams &p, const TcArgs &a, int n,
-                                const CUtensorMap &map, cudaStream_t stream);
+                                const CUtensorMap &map_k, const CUtensorMap &map_v,
+                                cudaStream_t stream);
 
 }  // namespace vae4

@@ -5,9 +5,10 @@
 namespace vae4 {
 
 cudaError_t launch_split_tc_dev(const SplitParams &p, const TcArgs &a, int n,
-                                const CUtensorMap &map, cudaStream_t stream) {
-  return p.hilo ? launch_tc_any<kPlanDevice, true>(p, a, n, map, stream)
-                : launch_tc_any<kPlanDevice, false>(p, a, n, map, stream);
+                                const CUtensorMap &map_k, const CUtensorMap &map_v,
+                                cudaStream_t stream) {
+  return p.hilo ? launch_tc_any<kPlanDevice, true>(p, a, n, map_k, map_v, stream)
+                : launch_tc_any<kPlanDevice, false>(p, a, n, map_k, map_v, stream);
 }
 
 }  // namespace vae4

@@ -7,9 +7,10 @@
 namespace vae4 {
 
 cudaError_t launch_split_tc_len(const SplitParams &p, const TcArgs &a, int n,
-                                const CUtensorMap &map, cudaStream_t stream) {
-  return p.hilo ? launch_tc_any<kPlanFromLen, true>(p, a, n, map, stream)
-                : launch_tc_any<kPlanFromLen, false>(p, a, n, map, stream);
+                                const CUtensorMap &map_k, const CUtensorMap &map_v,
+                                cudaStream_t stream) {
+  return p.hilo ? launch_tc_any<kPlanFromLen, true>(p, a, n, map_k, map_v, stream)
+                : launch_tc_any<kPlanFromLen, false>(p, a, n, map_k, map_v, stream);
 }
 
 }  // namespace vae4

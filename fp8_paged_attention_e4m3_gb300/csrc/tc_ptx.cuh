@@ -114,6 +114,37 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
 }
+// 5-D tensor load (c0 innermost) with an L2 cache-policy hint.
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                 int c2, int c3, int c4, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ------------------------------------------------- 8-byte asynchronous copies
+// Global -> shared, 8 bytes; src_bytes = 0 writes 8 zero bytes and reads
+// nothing.  L2 cache-policy hint as for the tensor loads.
+__device__ __forceinline__ void cp_async8_hint(uint32_t dst, const void *src, int src_bytes,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.ca.shared.global.L2::cache_hint [%0], [%1], 8, %2, %3;\n" ::"r"(dst), "l"(src),
+      "r"(src_bytes), "l"(policy)
+      : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (the arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

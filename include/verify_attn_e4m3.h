@@ -209,6 +209,35 @@ int verify_attn_e4m3_ex(const vae4_tensor *q, const vae4_tensor *kv_pages,
                         const vae4_options *opt);
 
 /*
+ * verify_attn_e4m3_kv -- the verify step over separate K and V caches in
+ * any strided layout, e.g. the token-major [blocks][block_size][kv_heads]
+ * [head_dim] caches of the pages, including padded token strides that are
+ * multiples of 8 but not of 16 bytes (the [1,848,1,256] view with strides
+ * [223872,264,256,1] of PR #524 "[Kernel][SM70] Add opt-in E4M3 grouped
+ * attention with FP32 partials", AI integration review and revision-2
+ * update).
+ *
+ *  k_cache, v_cache  U8 [n_pages][page][Hkv][D], the same shape; stride[3]
+ *              == 1; the other strides (in bytes, any order, K and V may
+ *              differ) non-negative multiples of 8; bases 8-byte aligned;
+ *              page = any multiple of 16 tokens up to 65536.  Token t of
+ *              sequence b, KV head h is k_cache[block_table[b][t / page]]
+ *              [t % page][h][:], and likewise in v_cache.
+ *  Other arguments, options, results and errors as verify_attn_e4m3_ex.
+ *
+ * When both caches have 16-byte aligned bases and strides that are
+ * multiples of 16 bytes (e.g. a contiguous token-major cache), their page
+ * slices are moved by tensor copies as for the pool; otherwise by 8-byte
+ * asynchronous copies (slower, same results).  The legacy mma.sync path
+ * (VAE4_FLAG_WARP_MMA) reads only the pool form: VAE4_ERR_UNSUPPORTED.
+ */
+int verify_attn_e4m3_kv(const vae4_tensor *q, const vae4_tensor *k_cache,
+                        const vae4_tensor *v_cache, const vae4_tensor *block_table,
+                        const vae4_tensor *seq_lens, const vae4_tensor *kv_scales,
+                        const vae4_tensor *out, const vae4_tensor *workspace,
+                        vae4_stream stream, const vae4_options *opt);
+
+/*
  * The two stages of verify_attn_e4m3, for callers that schedule them apart
  * (e.g. to time or overlap them).  Same arguments and contract.
  *   verify_attn_e4m3_partials: the split kernel only -- writes each live

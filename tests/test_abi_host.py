@@ -204,11 +204,72 @@ def test_validation_options(lib):
     assert _call(lib, a) == -1
 
 
-def test_stride_counterexample_is_rejected(lib):
-    """The pages' 8-but-not-16-byte token stride (264 B) cannot be expressed:
-    the pool must be contiguous, so each (page, K|V, head) slice starts on a
-    16-byte boundary; a 264-byte token stride is a stride error."""
+def test_stride_counterexample_is_rejected_by_the_pool_form(lib):
+    """The pool form [n_pages][2][Hkv][page][D] must be contiguous, so the
+    pages' 8-but-not-16-byte token stride (264 B) is a stride error there;
+    verify_attn_e4m3_kv takes that layout (next tests)."""
     g = GOLD["stride_counterexample"]
     assert g["strides"][1] == g["second_token_byte"] and g["second_token_byte"] % 16 == 8
     kv = _t(vae4.VAE4_U8, [80, 2, 1, 16, 256], [2 * 16 * 264, 16 * 264, 16 * 264, 264, 1])
     assert _call(lib, _args(kv=kv)) == -4
+
+
+# ------------------------------------- separate, strided K and V caches
+def _kv_args(k=None, v=None, **over):
+    """The pages' counterexample layout: [n][848][1][256], strides
+    [223872, 264, 256, 1] for both caches."""
+    g = GOLD["stride_counterexample"]
+    n = 40
+    shape, strides = [n] + g["shape"][1:], g["strides"]
+    a = _args(**over)
+    a["k"] = k or _t(vae4.VAE4_U8, shape, strides, data=FAKE * 8)
+    a["v"] = v or _t(vae4.VAE4_U8, shape, strides, data=FAKE * 16)
+    a["bt"] = _t(vae4.VAE4_I32, [1, 400])
+    return a
+
+
+def _call_kv(lib, a, opt=None):
+    o = opt or vae4.Options(0.0, 0, 0, 152, 0)
+    return lib.verify_attn_e4m3_kv(*[ctypes.byref(a[k]) for k in
+                                     ("q", "k", "v", "bt", "seq", "sc", "out", "ws")],
+                                   None, ctypes.byref(o))
+
+
+def test_kv_entry_accepts_the_counterexample_layout(lib):
+    """The [1,848,1,256] view with strides [223872,264,256,1] (PR #524, AI
+    integration review) passes every layout check: the call only fails on
+    the too-small workspace, which is checked after the caches."""
+    a = _kv_args(ws=_t(vae4.VAE4_U8, [1000], data=FAKE * 4))
+    assert _call_kv(lib, a) == -8
+    # a contiguous token-major cache (vLLM's layout) likewise
+    k = _t(vae4.VAE4_U8, [80, 16, 1, 256], data=FAKE * 8)
+    v = _t(vae4.VAE4_U8, [80, 16, 1, 256], data=FAKE * 16)
+    a = _kv_args(k=k, v=v, ws=_t(vae4.VAE4_U8, [1000], data=FAKE * 4))
+    a["bt"] = _t(vae4.VAE4_I32, [1, 64])
+    assert _call_kv(lib, a) == -8
+
+
+@pytest.mark.parametrize("which,bad,code", [
+    ("k", dict(strides=[223872, 260, 256, 1]), -4),   # not a multiple of 8
+    ("v", dict(strides=[223872, 264, 256, 2]), -4),   # d not contiguous
+    ("k", dict(data=FAKE * 8 + 4), -5),               # base not 8-byte aligned
+    ("v", dict(shape=[40, 848, 1, 128]), -3),         # D differs from q
+    ("k", dict(shape=[40, 840, 1, 256]), -3),         # K and V shapes differ
+    ("k", dict(dtype=vae4.VAE4_I32), -2),
+])
+def test_kv_entry_rejects(lib, which, bad, code):
+    g = GOLD["stride_counterexample"]
+    d = dict(shape=[40] + g["shape"][1:], strides=g["strides"], data=FAKE * 8,
+             dtype=vae4.VAE4_U8)
+    d.update(bad)
+    t = _t(d["dtype"], d["shape"], d["strides"], data=d["data"])
+    a = _kv_args(**{which: t})
+    assert _call_kv(lib, a) == code
+
+
+def test_kv_entry_page_size_and_flags(lib):
+    k = _t(vae4.VAE4_U8, [40, 40, 1, 256], [40 * 264, 264, 256, 1], data=FAKE * 8)
+    v = _t(vae4.VAE4_U8, [40, 40, 1, 256], [40 * 264, 264, 256, 1], data=FAKE * 16)
+    assert _call_kv(lib, _kv_args(k=k, v=v)) == -6    # page 40: not a multiple of 16
+    # the legacy mma.sync kernel reads the pool form only
+    assert _call_kv(lib, _kv_args(), vae4.Options(0.0, 0, 0, 152, vae4.FLAG_WARP_MMA)) == -6
