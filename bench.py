@@ -31,6 +31,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "µs per q8 verify step and KV-read GB/s (% of HBM peak) at 262144 ctx"
+GRAPH_STEPS = 20      # steps per captured graph
+SHAPES = ("tiny", "tp4", "long_q1", "tp2")  # other synthetic shapes, reported beside
+SHAPE_REPLAYS = 5
 WORKLOAD = "long"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -261,12 +264,15 @@ def main():
     with torch.cuda.stream(stream):  # warm the launch path on the capture stream
         vae4.verify(q, kvs[0], bt, seq, sc, out, ws, **kw)
     stream.synchronize()
+    # the K timed steps run as K / GS replays of a GS-step graph (each
+    # replay between its own events, so the spread over replays is known)
+    GS = GRAPH_STEPS if args.steps % GRAPH_STEPS == 0 else args.steps
     g_step, g_split = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
-        for k in range(args.steps):
+        for k in range(GS):
             vae4.verify(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
     with torch.cuda.graph(g_split, stream=stream):
-        for k in range(args.steps):
+        for k in range(GS):
             vae4.verify_attn_e4m3_partials(q, kvs[k % R], bt, seq, sc, out, ws, **kw)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):  # untimed replays: upload and first touch
@@ -274,26 +280,29 @@ def main():
         g_split.replay()
     torch.cuda.synchronize()
 
-    def timed(graph):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def timed(graph, n=1):
+        """ms of n back-to-back replays (barrier + synchronize on both sides)
+        and the ms of each replay"""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            e0.record()
-            graph.replay()
-            e1.record()
+            ev[0].record()
+            for i in range(n):
+                graph.replay()
+                ev[i + 1].record()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        return e0.elapsed_time(e1)
+        return ev[0].elapsed_time(ev[n]), [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
 
     uuid = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{uuid}" if uuid else None)
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-    total_ms = timed(g_step)
-    split_total_ms = timed(g_split)
+    total_ms, step_reps = timed(g_step, args.steps // GS)
+    split_total_ms, split_reps = timed(g_split, args.steps // GS)
     # ---- the step against the gather floor: the streaming-read kernel reads
     # exactly the step's KV bytes with plain loads and no compute.  Blocks of
     # KB launches, graph-replayed, A/B-interleaved (ABBA) after warm-up
@@ -314,7 +323,7 @@ def main():
     samp = {"a": [], "b": []}
     for i in range(NPAIR):
         for tag in (("a", "b") if i % 2 == 0 else ("b", "a")):
-            samp[tag].append(timed(g_a if tag == "a" else g_b) * 1e3 / KB)
+            samp[tag].append(timed(g_a if tag == "a" else g_b)[0] * 1e3 / KB)
     # ---- the paged FP8 -> FP16 bridge on the same cache: reads the KV bytes
     # once and writes them as dense FP16 (3 bytes moved per element)
     ko = torch.empty((s.B, s.Hkv, w.capacity, s.D), dtype=torch.float16, device=dev)
@@ -327,7 +336,7 @@ def main():
     with torch.cuda.stream(stream):
         g_br.replay()
     torch.cuda.synchronize()
-    bridge_us = timed(g_br) * 1e3 / NB
+    bridge_us = timed(g_br)[0] * 1e3 / NB
     del ko, vo, g_br
     # ---- ragged batch on the automatic plan (the device-side balanced plan):
     # 16 sequences of log-uniform lengths and mixed query counts in a launch
@@ -351,12 +360,48 @@ def main():
     with torch.cuda.stream(stream):
         g_rag.replay()
     torch.cuda.synchronize()
-    rag_us = timed(g_rag) * 1e3 / NRG
+    rag_us = timed(g_rag)[0] * 1e3 / NRG
     assert vae4.read_status(rws) == 0
     rag_bytes = wr.kv_bytes
     del rkvs, rkv, rws, g_rag
+    # ---- the other synthetic shapes, on the automatic plan (tiny: its 256-
+    # token partitions), each graph-replayed like the main leg
+    shapes = {}
+    for name in SHAPES:
+        ws_ = W.generate(name)
+        t_ = W.to_device(ws_, device=dev)
+        RS = max(1, math.ceil(3 * l2 / t_[1].numel()))
+        kv_s = [t_[1]] + [t_[1].clone() for _ in range(RS - 1)]
+        o_ = torch.zeros_like(t_[0])
+        sp = ws_.spec
+        w_ = vae4.alloc_workspace(sp.B, sp.Hq, sp.Hkv, sp.Qmax, sp.D, ws_.capacity,
+                                  sp.partition_tokens, device=dev)
+        kw_ = dict(partition_tokens=sp.partition_tokens, max_seq_len=ws_.capacity)
+        with torch.cuda.stream(stream):
+            vae4.verify(t_[0], kv_s[0], t_[2], t_[3], t_[4], o_, w_, **kw_)
+        stream.synchronize()
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_, stream=stream):
+            for k in range(GRAPH_STEPS):
+                vae4.verify(t_[0], kv_s[k % RS], t_[2], t_[3], t_[4], o_, w_, **kw_)
+        with torch.cuda.stream(stream):
+            g_.replay()
+        torch.cuda.synchronize()
+        _, reps = timed(g_, SHAPE_REPLAYS)
+        us = [r * 1e3 / GRAPH_STEPS for r in reps]
+        med = float(np.median(us))
+        shapes[name] = {"workload": workload_desc(ws_), "kv_bytes": ws_.kv_bytes,
+                        "us_median": med, "us_p90": float(np.percentile(us, 90)),
+                        "gbs": ws_.kv_bytes / (med * 1e-6) / 1e9,
+                        "frac": ws_.kv_bytes / (med * 1e-6) / 1e9 / peaks()[0],
+                        "l2": f"KV rotating over {RS} pool copies" if RS > 1 else
+                              "pool larger than 3x L2"}
+        assert vae4.read_status(w_) == 0
+        del kv_s, t_, o_, w_, g_, ws_
     clocks = sampler.stop()
     split_mean_us = split_total_ms * 1e3 / args.steps
+    step_rep_us = [r * 1e3 / GS for r in step_reps]
+    split_rep_us = [r * 1e3 / GS for r in split_reps]
     step_med, step_p90 = float(np.median(samp["a"])), float(np.percentile(samp["a"], 90))
     floor_med, floor_p90 = float(np.median(samp["b"])), float(np.percentile(samp["b"], 90))
     assert vae4.read_status(ws) == 0
@@ -401,7 +446,10 @@ def main():
         import oracle
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s",
-            "us_per_step": t_step * 1e3, "n_gpus": world, "steps": args.steps,
+            "us_per_step": t_step * 1e3,
+            "us_per_step_median": float(np.median(step_rep_us)),
+            "us_per_step_p90": float(np.percentile(step_rep_us, 90)),
+            "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "precision": {"kv": "e4m3", "operands": "f16", "state": "f32", "out": "f16"},
@@ -409,7 +457,8 @@ def main():
             "config": {"workload": workload_desc(w), "seed": s.seed,
                        "partition_tokens": T_eff, "partitions": P,
                        "plan": "automatic (one sequence: T from its length on the device)",
-                       "timing": f"{args.steps} steps in one CUDA graph replay",
+                       "timing": f"{args.steps} steps as {args.steps // GS} replays of a "
+                                 f"{GS}-step CUDA graph; median and p90 over the replays",
                        "l2": f"inputs rotate over {R} KV pool copies of {pool_bytes >> 20} MiB "
                              f"(> 3x the {l2 >> 20} MiB L2)"},
             "pct_of_hbm_peak": 100.0 * value / world / peak,
@@ -417,7 +466,10 @@ def main():
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                          "traffic": traffic, "split_us_mean": split_mean,
-                         "timing": f"{args.steps} back-to-back split launches in one CUDA graph"},
+                         "split_us_median": float(np.median(split_rep_us)),
+                         "split_us_p90": float(np.percentile(split_rep_us, 90)),
+                         "timing": f"{args.steps} back-to-back split launches as "
+                                   f"{args.steps // GS} replays of a {GS}-launch CUDA graph"},
             "cpu_baseline": {"value": kv_bytes / cpu_s / 1e9, "unit": "GB/s",
                              "cores": oracle.max_threads(), "kind": "oracle",
                              "sample": f"one full step: all {n_cpu} output rows, FP64",
@@ -446,6 +498,7 @@ def main():
                 "gbs": rag_bytes / (rag_us * 1e-6) / 1e9,
                 "frac": rag_bytes / (rag_us * 1e-6) / 1e9 / peak,
                 "timing": f"{NRG} steps in one CUDA graph replay, KV rotating over {RR} pool copies"},
+            "shapes": shapes,
             "gpu_launches": gpu_launches,
             "clocks": clocks,
             "gpu": props.name,

@@ -428,6 +428,7 @@ int prepare(const vae4_tensor *q, const vae4_tensor *kv, const vae4_tensor *kc,
   c.plan_N = n_rows;
   c.plan_tab = s.plan_tab;
   c.status = s.status;
+  c.num_sms = sms;
   return VAE4_OK;
 }
 

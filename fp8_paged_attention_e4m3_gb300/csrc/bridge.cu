@@ -13,8 +13,11 @@
 // from rounding p + e, since FP16 midpoints are FP32 numbers -- is broken
 // by the sign of e).  With the raw flag: dec(byte) itself (exact).
 //
-// One warp per (b, h, logical page): each lane converts 16 bytes (16
-// elements of one token) per step and stores 32 bytes; K and V interleaved.
+// One warp per (b, h, logical page) at a time: the page's K and V slices
+// are read in passes of 256 bytes (8 per lane, coalesced), eight passes per
+// round with every load in flight before the first conversion, and each
+// lane writes its 8 values as one 16-byte store (512 contiguous bytes per
+// warp instruction, streaming).
 #include "common.cuh"
 #include "kernels.h"
 #include "verify_attn_e4m3.h"
@@ -24,13 +27,16 @@ namespace vae4 {
 namespace {
 
 constexpr int kBridgeThreads = 256;
+constexpr int kRound = 8;  // 256-byte passes per round
 
 // fp16 of the exact product d * s (d exact in FP32), round to nearest even
 __device__ __forceinline__ __half mul_round_fp16(float d, float s) {
   const float p = d * s;
   const float e = fmaf(d, s, -p);  // p + e == d * s exactly
   const __half rn = __float2half_rn(p);
-  if (e == 0.f) return rn;
+  // p can only be an FP16 tie (the one case where rounding p differs from
+  // rounding p + e) if its 12 low fraction bits are zero
+  if (e == 0.f || (__float_as_uint(p) & 0xFFFu) != 0u) return rn;
   const __half lo = __float2half_rd(p), hi = __float2half_ru(p);
   if (__half_as_ushort(lo) == __half_as_ushort(hi)) return rn;  // p is an FP16 value
   const float mid = 0.5f * (__half2float(lo) + __half2float(hi));  // exact
@@ -38,11 +44,74 @@ __device__ __forceinline__ __half mul_round_fp16(float d, float s) {
   return e > 0.f ? hi : lo;
 }
 
+// FP8 byte b -> dec(b) * 2^-K exactly as an FP32 bit move: the magnitude
+// bits land in FP32 bits 26..20 (E4M3, K = 120) or 27..21 (E5M2, K = 112),
+// so the FP8 exponent field becomes the low bits of the FP32 one and FP8
+// subnormals become FP32 subnormals with the same significand.  (The
+// infinity and NaN codes, outside the contract, give finite values.)
+template <bool E5M2>
+__device__ __forceinline__ float fp8_to_f32_shifted(uint32_t b) {
+  return __uint_as_float(((b & 0x80u) << 24) | ((b & 0x7Fu) << (E5M2 ? 21 : 20)));
+}
+template <bool E5M2>
+constexpr float fp8_shift_scale() {  // 2^K
+  return E5M2 ? 5.192296858534828e+33f : 1.329227995784916e+36f;
+}
+
+// Scaled path: d' = dec(b) 2^-K and s' = s 2^K give the same exact product
+// d s, rounded to FP32 as p; two products go to FP16 with one conversion.
+// Rounding p instead of the exact product only differs at an FP16 tie,
+// which needs the 12 low fraction bits of p zero: those rare values take
+// mul_round_fp16.
+// Two products rounded to FP16 by one conversion; `tie` is set when either
+// could be an FP16 tie (those 8 values are redone by the exact path).
+template <bool E5M2>
+__device__ __forceinline__ uint32_t scaled_pair(uint32_t b0, uint32_t b1, float s2, bool &tie) {
+  const float p0 = fp8_to_f32_shifted<E5M2>(b0) * s2, p1 = fp8_to_f32_shifted<E5M2>(b1) * s2;
+  tie |= ((__float_as_uint(p0) & 0xFFFu) == 0u && p0 != 0.f) |
+         ((__float_as_uint(p1) & 0xFFFu) == 0u && p1 != 0.f);
+  const __half2 h = __floats2half2_rn(p0, p1);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// 8 FP8 bytes -> 8 FP16 values (scaled unless RAW); with SHIFT, sc is
+// s * 2^K and `tie` reports a possible FP16 tie among the 8
+template <bool E5M2, bool RAW, bool SHIFT>
+__device__ __forceinline__ uint4 convert8(uint2 raw, float sc, bool &tie) {
+  if constexpr (!RAW && SHIFT) {
+    const uint32_t x = raw.x, y = raw.y;
+    return make_uint4(scaled_pair<E5M2>(x & 0xFFu, (x >> 8) & 0xFFu, sc, tie),
+                      scaled_pair<E5M2>((x >> 16) & 0xFFu, x >> 24, sc, tie),
+                      scaled_pair<E5M2>(y & 0xFFu, (y >> 8) & 0xFFu, sc, tie),
+                      scaled_pair<E5M2>((y >> 16) & 0xFFu, y >> 24, sc, tie));
+  }
+  const uint32_t wds[2] = {raw.x, raw.y};
+  uint32_t hw[4];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const uint32_t h0 = fp8x2_to_f16x2<E5M2>(wds[e]);
+    const uint32_t h1 = fp8x2_to_f16x2<E5M2>(wds[e] >> 16);
+    if (RAW) {
+      hw[2 * e] = h0;
+      hw[2 * e + 1] = h1;
+    } else {
+      const __half2 a = *reinterpret_cast<const __half2 *>(&h0);
+      const __half2 c2 = *reinterpret_cast<const __half2 *>(&h1);
+      const __half2 ra = __halves2half2(mul_round_fp16(__low2float(a), sc),
+                                        mul_round_fp16(__high2float(a), sc));
+      const __half2 rc = __halves2half2(mul_round_fp16(__low2float(c2), sc),
+                                        mul_round_fp16(__high2float(c2), sc));
+      hw[2 * e] = *reinterpret_cast<const uint32_t *>(&ra);
+      hw[2 * e + 1] = *reinterpret_cast<const uint32_t *>(&rc);
+    }
+  }
+  return make_uint4(hw[0], hw[1], hw[2], hw[3]);
+}
+
 template <bool E5M2, bool RAW>
 __global__ void __launch_bounds__(kBridgeThreads) bridge_kernel(const BridgeParams p) {
   const int warps = gridDim.x * (kBridgeThreads / 32);
   const int w = blockIdx.x * (kBridgeThreads / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  const int cpt = p.D / 16;  // 16-byte chunks per token
   for (int b = 0; b < p.B; ++b) {
     const int L = p.seq[(int64_t)b * p.seq_sb];
     if (L < 0 || L > p.cap) {
@@ -57,49 +126,67 @@ __global__ void __launch_bounds__(kBridgeThreads) bridge_kernel(const BridgePara
       const bool ok_page = phys >= 0 && phys < p.n_pages;
       if (!ok_page && lane == 0 && p.status) atomicOr(p.status, VAE4_STATUS_BAD_BLOCK);
       const int toks = min(p.page, L - lp * p.page);
-      const float sk = RAW ? 1.f : p.scales[h * p.scale_sh + 0];
-      const float sv = RAW ? 1.f : p.scales[h * p.scale_sh + 1];
+      float sk = RAW ? 1.f : p.scales[h * p.scale_sh + 0];
+      float sv = RAW ? 1.f : p.scales[h * p.scale_sh + 1];
+      // pre-shifted scales for the bit-move decode, exact while finite
+      // (scales below 2^(127 - K)); otherwise the general path
+      const float sk2 = sk * fp8_shift_scale<E5M2>(), sv2 = sv * fp8_shift_scale<E5M2>();
+      const bool shift = !RAW && isfinite(sk2) && isfinite(sv2) && sk2 != 0.f && sv2 != 0.f;
+      if (shift) {
+        sk = sk2;
+        sv = sv2;
+      }
       const int64_t slice = (int64_t)p.page * p.D;
       const uint8_t *k = p.kv + ((int64_t)(ok_page ? phys : 0) * 2 * p.Hkv + h) * slice;
       const uint8_t *v = k + (int64_t)p.Hkv * slice;
-      uint16_t *ko = p.k_out + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh;
-      uint16_t *vo = p.v_out + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh;
-      const int nch = toks * cpt;
-      for (int c = lane; c < nch; c += 32) {
-        const int t = c / cpt, d0 = (c - t * cpt) * 16;
-        const int64_t orow = (int64_t)(lp * p.page + t) * p.o_st + d0;
-        uint4 rk = make_uint4(0, 0, 0, 0), rv = make_uint4(0, 0, 0, 0);
-        if (ok_page) {
-          rk = __ldcs(reinterpret_cast<const uint4 *>(k + (int64_t)c * 16));
-          rv = __ldcs(reinterpret_cast<const uint4 *>(v + (int64_t)c * 16));
-        }
+      uint16_t *ko = p.k_out + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh +
+                     (int64_t)lp * p.page * p.o_st;
+      uint16_t *vo = p.v_out + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh +
+                     (int64_t)lp * p.page * p.o_st;
+      const int nbytes = toks * p.D;  // bytes of this page's slice that are live
+      for (int base = 0; base < nbytes; base += kRound * 256) {
+        uint2 rk[kRound], rv[kRound];
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint4 raw = kv ? rv : rk;
-          const float sc = kv ? sv : sk;
-          const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t hw[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t h0 = fp8x2_to_f16x2<E5M2>(wds[e]);
-            const uint32_t h1 = fp8x2_to_f16x2<E5M2>(wds[e] >> 16);
-            if (RAW) {
-              hw[2 * e] = h0;
-              hw[2 * e + 1] = h1;
-            } else {
-              const __half2 a = *reinterpret_cast<const __half2 *>(&h0);
-              const __half2 c2 = *reinterpret_cast<const __half2 *>(&h1);
-              const __half2 ra = __halves2half2(mul_round_fp16(__low2float(a), sc),
-                                                mul_round_fp16(__high2float(a), sc));
-              const __half2 rc = __halves2half2(mul_round_fp16(__low2float(c2), sc),
-                                                mul_round_fp16(__high2float(c2), sc));
-              hw[2 * e] = *reinterpret_cast<const uint32_t *>(&ra);
-              hw[2 * e + 1] = *reinterpret_cast<const uint32_t *>(&rc);
-            }
+        for (int j = 0; j < kRound; ++j) {
+          const int off = base + 256 * j + 8 * lane;
+          rk[j] = rv[j] = make_uint2(0u, 0u);
+          if (ok_page && off < nbytes) {
+            rk[j] = __ldcs(reinterpret_cast<const uint2 *>(k + off));
+            rv[j] = __ldcs(reinterpret_cast<const uint2 *>(v + off));
           }
-          uint4 *dst = reinterpret_cast<uint4 *>((kv ? vo : ko) + orow);
-          __stcs(dst, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-          __stcs(dst + 1, make_uint4(hw[4], hw[5], hw[6], hw[7]));
+        }
+        uint32_t ties = 0;  // bit 2j (K) / 2j + 1 (V): redo with the exact path
+#pragma unroll
+        for (int j = 0; j < kRound; ++j) {
+          const int off = base + 256 * j + 8 * lane;
+          if (off < nbytes) {
+            const int t = off / p.D, d = off - t * p.D;
+            const int64_t o = (int64_t)t * p.o_st + d;
+            bool tk = false, tv = false;
+            if (shift) {
+              __stcs(reinterpret_cast<uint4 *>(ko + o), convert8<E5M2, RAW, true>(rk[j], sk, tk));
+              __stcs(reinterpret_cast<uint4 *>(vo + o), convert8<E5M2, RAW, true>(rv[j], sv, tv));
+            } else {
+              __stcs(reinterpret_cast<uint4 *>(ko + o), convert8<E5M2, RAW, false>(rk[j], sk, tk));
+              __stcs(reinterpret_cast<uint4 *>(vo + o), convert8<E5M2, RAW, false>(rv[j], sv, tv));
+            }
+            ties |= (tk ? 1u : 0u) << (2 * j) | (tv ? 1u : 0u) << (2 * j + 1);
+          }
+        }
+        if (!RAW && ties && ok_page) {
+          // rare: 8 values that may hold an FP16 tie, redone from their bytes
+          // with the exact rounding (the same thread rewrites what it wrote)
+          const float s_k = p.scales[h * p.scale_sh + 0], s_v = p.scales[h * p.scale_sh + 1];
+#pragma unroll 1
+          for (; ties; ties &= ties - 1) {
+            const int bit = __ffs(ties) - 1, j = bit >> 1, isv = bit & 1;
+            const int off = base + 256 * j + 8 * lane;
+            const int t = off / p.D, d = off - t * p.D;
+            const uint2 raw = __ldg(reinterpret_cast<const uint2 *>((isv ? v : k) + off));
+            bool unused = false;
+            __stcs(reinterpret_cast<uint4 *>((isv ? vo : ko) + (int64_t)t * p.o_st + d),
+                   convert8<E5M2, false, false>(raw, isv ? s_v : s_k, unused));
+          }
         }
       }
     }

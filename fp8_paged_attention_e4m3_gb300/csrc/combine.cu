@@ -1,19 +1,33 @@
-// Combine kernel: merges the FP32 partition states of each output row in
-// ascending partition order and writes the FP16 output.
+// Combine kernel: merges the FP32 partition states of each output row in a
+// fixed order and writes the FP16 output.
 //
 // For row r of (sequence b, KV head h), over the live partitions p (those
 // with p*T < L and a nonzero running sum):
 //     M   = max_p m_p                  (m_p in log2 units of the score)
 //     w_p = 2^(m_p - M)
 //     out = (sum_p w_p O_p) / (sum_p w_p l_p) * s_V * 2^8
-// all in FP32, rounded once to FP16 (round to nearest even), with a fixed
-// summation order.  It is the one place where the FP32 partition state
-// (max, sum, unnormalised P.V) is reduced, and it reduces in FP32 (PR #524
-// "[Kernel][SM70] Add opt-in E4M3 grouped attention with FP32 partials",
-// final status; PR #560 "[Bugfix] Use FP32 state and E4M3 defaults for
-// DFlash2", Purpose).
+// all in FP32, rounded once to FP16 (round to nearest even).  It is the one
+// place where the FP32 partition state (max, sum, unnormalised P.V) is
+// reduced, and it reduces in FP32 (PR #524 "[Kernel][SM70] Add opt-in E4M3
+// grouped attention with FP32 partials", final status; PR #560 "[Bugfix]
+// Use FP32 state and E4M3 defaults for DFlash2", Purpose).
 // Padding query slots, dead sequences (L == 0) and sequences whose lengths
 // or pages were invalid get zeros.
+//
+// Work decomposition: a unit is (live row, 32-wide slice of d), taken by
+// WPU warps (one, or four when each stream has many partitions).  Lane =
+// (partition group, float4 of the slice): eight lanes read 128 contiguous
+// bytes of one partition's O, four groups per warp, 4 * WPU groups per unit;
+// group g takes partitions g, g + 4 WPU, ... in ascending order and loads
+// their (max, sum) pairs itself (its eight lanes share the address).  The
+// group sums are added by a fixed shuffle tree within a warp and, with four
+// warps, in warp order, so the summation order depends only on the
+// partition count, never on scheduling: repeated runs agree bit for bit.
+// Units are taken in a grid-stride loop over the launch's capacity
+// (B x Hkv x Qmax*G rows x D/32 slices); rows without a live query are
+// skipped at once, so a batch of short query counts costs no waves of idle
+// blocks, and are zero-filled before the grid dependency wait (the split
+// kernel does not touch the output).
 #include "common.cuh"
 #include "kernels.h"
 #include "plan.cuh"
@@ -23,22 +37,52 @@ namespace vae4 {
 
 namespace {
 
-constexpr int kCombineThreads = 256;
-constexpr int kLanes = 16;                          // float4 lanes: 64 d per CTA
-constexpr int kGroups = kCombineThreads / kLanes;   // partition groups
+// One block of 16 warps per SM (its registers leave room for no second
+// block): the blocks are placed as the split kernel's CTAs leave their SMs,
+// and smaller blocks piled up on the first SMs to free up (half the SMs
+// took every block of the long-context step).
+constexpr int kCombineThreads = 512;
+constexpr int kWarps = kCombineThreads / 32;
+constexpr int kCacheB = 2048;   // lengths cached in shared memory up to this batch
+constexpr int kCacheTab = 2048; // device-plan stream entries cached up to this many
 
-// One CTA per (output row, 64-wide slice of d).  Every CTA of a row computes
+struct Len {
+  int L, ql;
+};
+
+__device__ __forceinline__ Len read_len(const CombineParams &p, int b) {
+  const int L = p.seq[(int64_t)b * p.seq_sb];
+  const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
+  return Len{L, ql};
+}
+
+// barrier of the WPU warps of one unit (named barrier 1 + unit in block)
+__device__ __forceinline__ void unit_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// a row (query i) of sequence b holds a live query
+__device__ __forceinline__ bool live_row(const CombineParams &p, Len l, int i) {
+  return l.L > 0 && l.L <= p.capacity && l.ql >= 0 && l.ql <= p.Qmax && l.ql <= l.L && i < l.ql;
+}
+
+constexpr int kRowThreads = 256;
+constexpr int kRowLanes = 16;                         // float4 lanes: 64 d per CTA
+constexpr int kRowGroups = kRowThreads / kRowLanes;   // partition groups
+
+// Static plans whose streams spread over many partitions (one sequence over
+// every SM): one CTA per (output row, 64-wide slice of d).  Every CTA of a row computes
 // the row's partition weights into shared memory (a few hundred floats);
-// the P.V partials of its slice are then summed by kGroups groups of
-// threads, group k taking partitions k, k + kGroups, ... in ascending order,
+// the P.V partials of its slice are then summed by kRowGroups groups of
+// threads, group k taking partitions k, k + kRowGroups, ... in ascending order,
 // and the group sums are added in group order: a fixed summation order that
 // does not depend on scheduling, so repeated runs agree bit for bit.  Many
 // short independent loads per thread keep the L2 busy instead of waiting on
 // one long dependent chain.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
-  extern __shared__ __align__(16) float csm[];
-  __shared__ float red[kCombineThreads / 32];
-  __shared__ float4 accs[kGroups][kLanes];
+__global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const CombineParams p) {
+  extern __shared__ __align__(16) float rsm[];
+  __shared__ float red[kRowThreads / 32];
+  __shared__ float4 accs[kRowGroups][kRowLanes];
 
   const int nd = p.D / 64;  // d slices per row
   const int r = blockIdx.x / nd, dsl = blockIdx.x - r * nd;
@@ -80,22 +124,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     }
   }
   if (dead) nP = 0;
-  float *wm = csm;       // m_p, then the weight w_p
-  float *wl = csm + p.P; // l_p
+  float *wm = rsm;       // m_p, then the weight w_p
+  float *wl = rsm + p.P; // l_p
   const int64_t pstride = (int64_t)p.rows_pad;  // rows per partition
   const float *ml = p.ws_ml + (int64_t)slot0 * pstride * 2 + r * 2;
   const float kNegInf = -__int_as_float(0x7f800000);
 
   // the first kPre P.V partials of this thread's group are requested now,
   // together with the (m, l) pairs, so both L2 round trips overlap
-  const int l4 = tid % kLanes, grp = tid / kLanes;
+  const int l4 = tid % kRowLanes, grp = tid / kRowLanes;
   const float *o = p.ws_o + (int64_t)slot0 * pstride * p.D + (int64_t)r * p.D + d0 + 4 * l4;
   const int64_t ostride = pstride * p.D;
   constexpr int kPre = 10;  // covers 160 partitions
   float4 pre[kPre];
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
-    const int q = grp + k * kGroups;
+    const int q = grp + k * kRowGroups;
     pre[k] = q < nP ? __ldcg(reinterpret_cast<const float4 *>(o + q * ostride))
                     : make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -103,7 +147,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   // ---- pass 1: (m_p, l_p), maximum over partitions with l_p > 0
   float mx = kNegInf;
   bool bad = false;
-  for (int q = tid; q < nP; q += kCombineThreads) {
+  for (int q = tid; q < nP; q += kRowThreads) {
     const float2 v = *reinterpret_cast<const float2 *>(ml + q * pstride * 2);
     wm[q] = v.x;
     wl[q] = v.y;
@@ -116,12 +160,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   const bool any_bad = __syncthreads_or(bad);
   float M = red[0];
 #pragma unroll
-  for (int k = 1; k < kCombineThreads / 32; ++k) M = fmaxf(M, red[k]);
+  for (int k = 1; k < kRowThreads / 32; ++k) M = fmaxf(M, red[k]);
   __syncthreads();
 
   // ---- pass 2: weights w_p = 2^(m_p - M) and the total sum (fixed tree)
   float lam = 0.f;
-  for (int q = tid; q < nP; q += kCombineThreads) {
+  for (int q = tid; q < nP; q += kRowThreads) {
     const float l = wl[q];
     const float w = l > 0.f ? (wm[q] == M ? 1.f : exp2f(wm[q] - M)) : 0.f;
     wm[q] = w;
@@ -133,14 +177,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   __syncthreads();
   float Lam = 0.f;
 #pragma unroll
-  for (int k = 0; k < kCombineThreads / 32; ++k) Lam += red[k];
+  for (int k = 0; k < kRowThreads / 32; ++k) Lam += red[k];
 
   // ---- pass 3: sum of w_p * O_p over this slice, per group (ascending p),
   // then over groups
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
-    const int q = grp + k * kGroups;
+    const int q = grp + k * kRowGroups;
     if (q < nP) {
       const float w = wm[q];
       acc.x += w * pre[k].x;
@@ -150,7 +194,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     }
   }
 #pragma unroll 4
-  for (int q = grp + kPre * kGroups; q < nP; q += kGroups) {
+  for (int q = grp + kPre * kRowGroups; q < nP; q += kRowGroups) {
     const float w = wm[q];
     const float4 v = __ldcg(reinterpret_cast<const float4 *>(o + q * ostride));
     acc.x += w * v.x;
@@ -163,7 +207,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   if (grp != 0) return;
   float4 s = accs[0][l4];
 #pragma unroll
-  for (int k = 1; k < kGroups; ++k) {
+  for (int k = 1; k < kRowGroups; ++k) {
     const float4 v = accs[k][l4];
     s.x += v.x;
     s.y += v.y;
@@ -179,6 +223,226 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
     res.y = *reinterpret_cast<const uint32_t *>(&hi);
   }
   *reinterpret_cast<uint2 *>(out + 4 * l4) = res;
+}
+
+template <int WPU>
+__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const CombineParams p) {
+  constexpr int PG = 4 * WPU;             // partition groups per unit
+  constexpr int NPL = WPU == 1 ? 8 : 10;  // partitions per lane per chunk
+  constexpr int CH = PG * NPL;            // partitions per chunk
+  constexpr int UPB = kWarps / WPU;       // units per block and pass
+  static_assert(WPU == 1 || UPB <= 15, "one named barrier per unit");
+  extern __shared__ __align__(16) int csm[];
+  __shared__ float4 xw[kWarps][8];        // four-warp units: per-warp sums
+  __shared__ float xm[kWarps], xl[kWarps];
+  const int nb_cache = p.B <= kCacheB ? p.B : 0;
+  int2 *lens = reinterpret_cast<int2 *>(csm);           // (L, q_len) per sequence
+  int2 *tab = reinterpret_cast<int2 *>(csm) + nb_cache;  // (first slot, partitions)
+  const int ntab = (p.dev_plan && p.B * p.Hkv <= kCacheTab) ? p.B * p.Hkv : 0;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int R = p.Qmax * p.G;  // rows per (sequence, KV head)
+  const int S = p.D / 32;      // slices per row
+
+  // ---- before the grid dependency wait: inputs only.  Lengths into shared
+  // memory; rows without a live query zero-filled; invalid lengths reported.
+  for (int b = tid; b < nb_cache; b += kCombineThreads) {
+    const Len l = read_len(p, b);
+    lens[b] = make_int2(l.L, l.ql);
+  }
+  __syncthreads();
+  auto len_of = [&](int b) -> Len {
+    if (b < nb_cache) return Len{lens[b].x, lens[b].y};
+    return read_len(p, b);
+  };
+  {
+    // 16 bytes (8 halves) per thread over every output row of a query slot
+    // that is not live
+    const int per_row = p.D / 8;
+    const int64_t n = (int64_t)p.B * p.Qmax * p.Hq * per_row;
+    for (int64_t x = (int64_t)blockIdx.x * kCombineThreads + tid; x < n;
+         x += (int64_t)gridDim.x * kCombineThreads) {
+      const int c = (int)(x % per_row);
+      const int64_t rw = x / per_row;
+      const int hq = (int)(rw % p.Hq);
+      const int i = (int)((rw / p.Hq) % p.Qmax);
+      const int b = (int)(rw / ((int64_t)p.Hq * p.Qmax));
+      if (!live_row(p, len_of(b), i)) {
+        __half *o = static_cast<__half *>(p.out) + (int64_t)b * p.o_sb + (int64_t)i * p.o_si +
+                    (int64_t)hq * p.o_sh + 8 * c;
+        *reinterpret_cast<uint4 *>(o) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    if (blockIdx.x == 0) {  // report invalid lengths once per sequence
+      for (int b = tid; b < p.B; b += kCombineThreads) {
+        const Len l = len_of(b);
+        if (l.L < 0 || l.L > p.capacity)
+          atomicOr(p.status, VAE4_STATUS_BAD_LENGTH);
+        else if (l.ql < 0 || l.ql > p.Qmax || (l.L > 0 && l.ql > l.L))
+          atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
+      }
+    }
+  }
+
+  // ---- wait until the split kernel's partials are complete and visible
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  for (int e = tid; e < ntab; e += kCombineThreads) tab[e] = p.plan_tab[e];
+  __syncthreads();
+
+  const float kNegInf = -__int_as_float(0x7f800000);
+  const int uw = warp / WPU, wi = warp % WPU;  // unit within the block, warp within the unit
+  const int g = wi * 4 + (lane >> 3), f = lane & 7;
+  const int64_t nunits = (int64_t)p.B * p.Hkv * R * S;
+  // units interleaved over the blocks (block x takes x, x + grid, ...), so
+  // every SM gets a share; the pass count is the same for all warps of a
+  // block (block barriers inside four-warp units)
+  const int64_t per_pass = (int64_t)gridDim.x * UPB;
+  for (int64_t u0 = 0; u0 < nunits; u0 += per_pass) {
+    const int64_t u = u0 + (int64_t)uw * gridDim.x + blockIdx.x;
+    bool live = u < nunits;
+    int s = 0, r = 0, h = 0, b = 0, i = 0, gg = 0;
+    Len l{0, 0};
+    if (live) {
+      // unit -> (b, h, row, slice); slices fastest
+      s = (int)(u % S);
+      const int64_t ur = u / S;
+      r = (int)(ur % R);
+      const int64_t bh = ur / R;
+      h = (int)(bh % p.Hkv);
+      b = (int)(bh / p.Hkv);
+      i = r / p.G;
+      gg = r - i * p.G;
+      l = len_of(b);
+      live = live_row(p, l, i);
+    }
+    if (WPU == 1 && !live) continue;  // zero-filled above (uniform per warp)
+    // partitions of this (sequence, KV head): slots slot0 .. slot0 + nP - 1
+    int slot0 = 0, nP = 0;
+    if (live) {
+      if (!p.dev_plan) {
+        slot0 = (b * p.Hkv + h) * p.P;
+        const int T = p.t_from_len ? max(64, plan_t_from_len(l.L, p.P)) : p.T;
+        nP = (l.L + T - 1) / T;
+      } else {
+        const int2 e = b * p.Hkv + h < ntab ? tab[b * p.Hkv + h] : p.plan_tab[b * p.Hkv + h];
+        slot0 = e.x;
+        nP = e.y;
+        if (slot0 < 0 || nP < 1 || nP > p.P || slot0 + nP > p.plan_G) {  // never: a library bug
+          if (lane == 0 && wi == 0) atomicOr(p.status, VAE4_STATUS_PLAN);
+          nP = 0;
+        }
+      }
+    }
+    const int64_t pstride = (int64_t)p.rows_pad;  // rows per partition slot
+    const float *ml = p.ws_ml + ((int64_t)slot0 * pstride + r) * 2;
+    const float *o = p.ws_o + ((int64_t)slot0 * pstride + r) * p.D + 32 * s + 4 * f;
+    const int64_t ostride = pstride * p.D;
+
+    float M = kNegInf, lam = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool bad = false;
+    for (int c0 = 0; c0 < nP; c0 += CH) {
+      // this lane's partitions q = c0 + g + PG k: (max, sum) pairs first,
+      // then the O partials, all in flight together
+      float2 mlr[NPL];
+      float4 v[NPL];
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) {
+        const int q = c0 + g + PG * k;
+        mlr[k] = q < nP ? __ldcg(reinterpret_cast<const float2 *>(ml + (int64_t)q * pstride * 2))
+                        : make_float2(kNegInf, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) {
+        const int q = c0 + g + PG * k;
+        v[k] = q < nP ? __ldcg(reinterpret_cast<const float4 *>(o + (int64_t)q * ostride))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      // maximum over live partitions (l > 0); a negative sum marks a
+      // partition that met an invalid page or timed out
+      float mx = M;
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) {
+        if (mlr[k].y > 0.f) mx = fmaxf(mx, mlr[k].x);
+        bad |= mlr[k].y < 0.f;
+      }
+#pragma unroll
+      for (int off = 8; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if constexpr (WPU > 1) {  // the unit's warps take part in the same chunks
+        if (lane == 0) xm[warp] = mx;
+        unit_bar(1 + uw, 32 * WPU);
+#pragma unroll
+        for (int w = 0; w < WPU; ++w) mx = fmaxf(mx, xm[uw * WPU + w]);
+        unit_bar(1 + uw, 32 * WPU);
+      }
+      if (mx != M) {  // this chunk raised the maximum: rescale the sums so far
+        const float c = M == kNegInf ? 0.f : exp2f(M - mx);
+        lam *= c;
+        acc.x *= c;
+        acc.y *= c;
+        acc.z *= c;
+        acc.w *= c;
+        M = mx;
+      }
+      // w = 2^(m - M); sums over this lane's partitions in ascending order
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) {
+        const float w = mlr[k].y > 0.f ? (mlr[k].x == M ? 1.f : exp2f(mlr[k].x - M)) : 0.f;
+        lam += w * mlr[k].y;
+        acc.x += w * v[k].x;
+        acc.y += w * v[k].y;
+        acc.z += w * v[k].z;
+        acc.w += w * v[k].w;
+      }
+    }
+    // the four partition groups of the warp, by a fixed tree (lane bits 3, 4)
+#pragma unroll
+    for (int off = 8; off < 32; off <<= 1) {
+      lam += __shfl_xor_sync(0xffffffffu, lam, off);
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if constexpr (WPU > 1) {  // then the unit's warps, in warp order
+      if (lane < 8) xw[warp][lane] = acc;
+      if (lane == 0) {
+        xl[warp] = lam;
+        xm[warp] = bad ? 1.f : 0.f;
+      }
+      unit_bar(1 + uw, 32 * WPU);
+      if (wi == 0 && lane < 8) {
+        acc = xw[uw * WPU][lane];
+        lam = xl[uw * WPU];
+        bad = xm[uw * WPU] != 0.f;
+#pragma unroll
+        for (int w = 1; w < WPU; ++w) {
+          const float4 a = xw[uw * WPU + w][lane];
+          acc.x += a.x;
+          acc.y += a.y;
+          acc.z += a.z;
+          acc.w += a.w;
+          lam += xl[uw * WPU + w];
+          bad |= xm[uw * WPU + w] != 0.f;
+        }
+      }
+      unit_bar(1 + uw, 32 * WPU);
+    }
+    if (live && wi == 0 && lane < 8) {
+      uint2 res = make_uint2(0u, 0u);
+      if (!bad && lam > 0.f) {
+        const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // partials hold dec(V) * 2^-8
+        const __half2 lo = __floats2half2_rn(__fdiv_rn(acc.x, lam) * beta, __fdiv_rn(acc.y, lam) * beta);
+        const __half2 hi = __floats2half2_rn(__fdiv_rn(acc.z, lam) * beta, __fdiv_rn(acc.w, lam) * beta);
+        res.x = *reinterpret_cast<const uint32_t *>(&lo);
+        res.y = *reinterpret_cast<const uint32_t *>(&hi);
+      }
+      __half *out = static_cast<__half *>(p.out) + (int64_t)b * p.o_sb + (int64_t)i * p.o_si +
+                    (int64_t)(h * p.G + gg) * p.o_sh + 32 * s + 4 * f;
+      *reinterpret_cast<uint2 *>(out) = res;
+    }
+  }
 }
 
 __global__ void decode_table_kernel(uint16_t *out, bool integer_path, bool e5m2) {
@@ -203,24 +467,48 @@ __global__ void decode_table_kernel(uint16_t *out, bool integer_path, bool e5m2)
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
-  if (p.D % 64 != 0) return cudaErrorInvalidValue;
+  if (p.D % 32 != 0) return cudaErrorInvalidValue;
+  if (!p.dev_plan && p.P > 32) {  // one stream over many partitions: a CTA per (row, 64 d)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.Qmax * p.G * (p.D / 64), p.Hkv, p.B);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float);  // (m_p, l_p) per partition
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int smem = (int)cfg.dynamicSmemBytes;
+    if (smem > 48 * 1024) {  // beyond the default dynamic shared-memory limit
+      const cudaError_t e = cudaFuncSetAttribute(combine_rows_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaLaunchKernelEx(&cfg, combine_rows_kernel, p);
+  }
+  const int WPU = 1;
+  // enough blocks for every unit of the launch's capacity, at most the
+  // resident blocks of one wave (units past it: grid-stride loop)
+  const int64_t units = (int64_t)p.B * p.Hkv * p.Qmax * p.G * (p.D / 32);
+  const int64_t cap = p.num_sms > 0 ? p.num_sms : 148;  // one block per SM
+  const int upb = kWarps / WPU;
+  int64_t nblk = (units + upb - 1) / upb;
+  nblk = nblk < 1 ? 1 : (nblk > cap ? cap : nblk);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.Qmax * p.G * (p.D / 64), p.Hkv, p.B);
+  cfg.gridDim = dim3((unsigned)nblk, 1, 1);
   cfg.blockDim = dim3(kCombineThreads);
-  cfg.dynamicSmemBytes = (size_t)p.P * 2 * sizeof(float);  // (m_p, l_p) per partition
+  const int nb_cache = p.B <= kCacheB ? p.B : 0;
+  const int ntab = (p.dev_plan && p.B * p.Hkv <= kCacheTab) ? p.B * p.Hkv : 0;
+  cfg.dynamicSmemBytes = (size_t)(nb_cache + ntab) * sizeof(int2);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int smem = (int)cfg.dynamicSmemBytes;
-  if (smem > 48 * 1024) {  // beyond the default dynamic shared-memory limit
-    const cudaError_t e =
-        cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+  return WPU == 4 ? cudaLaunchKernelEx(&cfg, combine_kernel<4>, p)
+                  : cudaLaunchKernelEx(&cfg, combine_kernel<1>, p);
 }
 
 cudaError_t launch_decode_table(uint16_t *out, bool integer_path, bool e5m2,

@@ -67,6 +67,7 @@ struct CombineParams {
   const int2 *plan_tab;      // device plan: (first slot, partitions) [B][Hkv]
   int32_t t_from_len;        // static grid, T from each sequence's length
   uint32_t *status;
+  int32_t num_sms;           // SMs the grid is sized for
 };
 
 // The bridge kernel's parameters (paged FP8 -> dense FP16 K and V).

@@ -420,8 +420,9 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
     ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
     if constexpr (MODE == kPlanFromLen) {
       // the sequence's P partitions share its L tokens; the block table is
-      // read once the length is known (fetching a guessed window first and
-      // fetching again when it misses cost more registers than it saved)
+      // read once the length is known (fetching the window of the plan at
+      // the capacity first, with a second fetch on a miss, measured no
+      // earlier first data and a slightly slower kernel)
       if (L > 0 && L <= p.capacity) T = max(64, plan_t_from_len(L, p.P));
       fetch_bt(b, part * T);
     }
