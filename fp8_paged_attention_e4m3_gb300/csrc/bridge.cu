@@ -8,16 +8,19 @@
 //
 // Value written: fp16(dec(byte) * s) with s the head's FP32 K or V scale,
 // rounded once from the exact product (dec(byte) has at most 4 significant
-// bits, s 24: the FP32 product p may be inexact, but its error e is exact
-// from an FMA; an FP16 tie at p -- the only case where rounding p differs
-// from rounding p + e, since FP16 midpoints are FP32 numbers -- is broken
-// by the sign of e).  With the raw flag: dec(byte) itself (exact).
+// bits, s 24, so the FP32 product may be inexact): the product is rounded
+// to FP32 to odd and then to FP16 to nearest even (see mul_round_to_odd);
+// scales too large for that path's pre-shift take mul_round_fp16 instead,
+// which breaks an FP16 tie at the FP32 product by the sign of its exact FMA
+// residual.  With the raw flag: dec(byte) itself (exact).
 //
 // One warp per (b, h, logical page) at a time: the page's K and V slices
 // are read in passes of 256 bytes (8 per lane, coalesced), eight passes per
 // round with every load in flight before the first conversion, and each
 // lane writes its 8 values as one 16-byte store (512 contiguous bytes per
 // warp instruction, streaming).
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "verify_attn_e4m3.h"
@@ -59,31 +62,36 @@ constexpr float fp8_shift_scale() {  // 2^K
 }
 
 // Scaled path: d' = dec(b) 2^-K and s' = s 2^K give the same exact product
-// d s, rounded to FP32 as p; two products go to FP16 with one conversion.
-// Rounding p instead of the exact product only differs at an FP16 tie,
-// which needs the 12 low fraction bits of p zero: those rare values take
-// mul_round_fp16.
-// Two products rounded to FP16 by one conversion; `tie` is set when either
-// could be an FP16 tie (those 8 values are redone by the exact path).
+// d s.  It is rounded to FP32 *to odd* (toward zero, then the last bit set
+// if anything was cut off, which the FMA residual tells), and that value to
+// FP16 to nearest even: since FP32 carries at least two more bits than FP16
+// (also for FP16 subnormal results), the two roundings give exactly the
+// single rounding of d s (Boldo and Melquiond, "When double rounding is
+// odd", 2005; "Emulation of FMA and correctly rounded sums: proved
+// algorithms using rounding to odd", IEEE Trans. Computers 2008).  Two
+// products go to FP16 in one conversion; no branch.
+__device__ __forceinline__ float mul_round_to_odd(float d, float s) {
+  const float r = __fmul_rz(d, s);
+  const float e = __fmaf_rn(d, s, -r);  // d s - r, exact
+  return __uint_as_float(__float_as_uint(r) | (e != 0.f ? 1u : 0u));
+}
 template <bool E5M2>
-__device__ __forceinline__ uint32_t scaled_pair(uint32_t b0, uint32_t b1, float s2, bool &tie) {
-  const float p0 = fp8_to_f32_shifted<E5M2>(b0) * s2, p1 = fp8_to_f32_shifted<E5M2>(b1) * s2;
-  tie |= ((__float_as_uint(p0) & 0xFFFu) == 0u && p0 != 0.f) |
-         ((__float_as_uint(p1) & 0xFFFu) == 0u && p1 != 0.f);
+__device__ __forceinline__ uint32_t scaled_pair(uint32_t b0, uint32_t b1, float s2) {
+  const float p0 = mul_round_to_odd(fp8_to_f32_shifted<E5M2>(b0), s2);
+  const float p1 = mul_round_to_odd(fp8_to_f32_shifted<E5M2>(b1), s2);
   const __half2 h = __floats2half2_rn(p0, p1);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// 8 FP8 bytes -> 8 FP16 values (scaled unless RAW); with SHIFT, sc is
-// s * 2^K and `tie` reports a possible FP16 tie among the 8
+// 8 FP8 bytes -> 8 FP16 values (scaled unless RAW); with SHIFT, sc is s * 2^K
 template <bool E5M2, bool RAW, bool SHIFT>
-__device__ __forceinline__ uint4 convert8(uint2 raw, float sc, bool &tie) {
+__device__ __forceinline__ uint4 convert8(uint2 raw, float sc) {
   if constexpr (!RAW && SHIFT) {
     const uint32_t x = raw.x, y = raw.y;
-    return make_uint4(scaled_pair<E5M2>(x & 0xFFu, (x >> 8) & 0xFFu, sc, tie),
-                      scaled_pair<E5M2>((x >> 16) & 0xFFu, x >> 24, sc, tie),
-                      scaled_pair<E5M2>(y & 0xFFu, (y >> 8) & 0xFFu, sc, tie),
-                      scaled_pair<E5M2>((y >> 16) & 0xFFu, y >> 24, sc, tie));
+    return make_uint4(scaled_pair<E5M2>(x & 0xFFu, (x >> 8) & 0xFFu, sc),
+                      scaled_pair<E5M2>((x >> 16) & 0xFFu, x >> 24, sc),
+                      scaled_pair<E5M2>(y & 0xFFu, (y >> 8) & 0xFFu, sc),
+                      scaled_pair<E5M2>((y >> 16) & 0xFFu, y >> 24, sc));
   }
   const uint32_t wds[2] = {raw.x, raw.y};
   uint32_t hw[4];
@@ -144,51 +152,36 @@ __global__ void __launch_bounds__(kBridgeThreads) bridge_kernel(const BridgePara
       uint16_t *vo = p.v_out + (int64_t)b * p.o_sb + (int64_t)h * p.o_sh +
                      (int64_t)lp * p.page * p.o_st;
       const int nbytes = toks * p.D;  // bytes of this page's slice that are live
-      for (int base = 0; base < nbytes; base += kRound * 256) {
-        uint2 rk[kRound], rv[kRound];
+      // one copy of the loop per conversion path (the choice is per page)
+      auto rounds = [&](auto shift_tag) {
+        constexpr bool SH = decltype(shift_tag)::value;
+        for (int base = 0; base < nbytes; base += kRound * 256) {
+          uint2 rk[kRound], rv[kRound];
 #pragma unroll
-        for (int j = 0; j < kRound; ++j) {
-          const int off = base + 256 * j + 8 * lane;
-          rk[j] = rv[j] = make_uint2(0u, 0u);
-          if (ok_page && off < nbytes) {
-            rk[j] = __ldcs(reinterpret_cast<const uint2 *>(k + off));
-            rv[j] = __ldcs(reinterpret_cast<const uint2 *>(v + off));
-          }
-        }
-        uint32_t ties = 0;  // bit 2j (K) / 2j + 1 (V): redo with the exact path
-#pragma unroll
-        for (int j = 0; j < kRound; ++j) {
-          const int off = base + 256 * j + 8 * lane;
-          if (off < nbytes) {
-            const int t = off / p.D, d = off - t * p.D;
-            const int64_t o = (int64_t)t * p.o_st + d;
-            bool tk = false, tv = false;
-            if (shift) {
-              __stcs(reinterpret_cast<uint4 *>(ko + o), convert8<E5M2, RAW, true>(rk[j], sk, tk));
-              __stcs(reinterpret_cast<uint4 *>(vo + o), convert8<E5M2, RAW, true>(rv[j], sv, tv));
-            } else {
-              __stcs(reinterpret_cast<uint4 *>(ko + o), convert8<E5M2, RAW, false>(rk[j], sk, tk));
-              __stcs(reinterpret_cast<uint4 *>(vo + o), convert8<E5M2, RAW, false>(rv[j], sv, tv));
-            }
-            ties |= (tk ? 1u : 0u) << (2 * j) | (tv ? 1u : 0u) << (2 * j + 1);
-          }
-        }
-        if (!RAW && ties && ok_page) {
-          // rare: 8 values that may hold an FP16 tie, redone from their bytes
-          // with the exact rounding (the same thread rewrites what it wrote)
-          const float s_k = p.scales[h * p.scale_sh + 0], s_v = p.scales[h * p.scale_sh + 1];
-#pragma unroll 1
-          for (; ties; ties &= ties - 1) {
-            const int bit = __ffs(ties) - 1, j = bit >> 1, isv = bit & 1;
+          for (int j = 0; j < kRound; ++j) {
             const int off = base + 256 * j + 8 * lane;
-            const int t = off / p.D, d = off - t * p.D;
-            const uint2 raw = __ldg(reinterpret_cast<const uint2 *>((isv ? v : k) + off));
-            bool unused = false;
-            __stcs(reinterpret_cast<uint4 *>((isv ? vo : ko) + (int64_t)t * p.o_st + d),
-                   convert8<E5M2, false, false>(raw, isv ? s_v : s_k, unused));
+            rk[j] = rv[j] = make_uint2(0u, 0u);
+            if (ok_page && off < nbytes) {
+              rk[j] = __ldcs(reinterpret_cast<const uint2 *>(k + off));
+              rv[j] = __ldcs(reinterpret_cast<const uint2 *>(v + off));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kRound; ++j) {
+            const int off = base + 256 * j + 8 * lane;
+            if (off < nbytes) {
+              const int t = off / p.D, d = off - t * p.D;
+              const int64_t o = (int64_t)t * p.o_st + d;
+              __stcs(reinterpret_cast<uint4 *>(ko + o), convert8<E5M2, RAW, SH>(rk[j], sk));
+              __stcs(reinterpret_cast<uint4 *>(vo + o), convert8<E5M2, RAW, SH>(rv[j], sv));
+            }
           }
         }
-      }
+      };
+      if (shift)
+        rounds(std::true_type{});
+      else
+        rounds(std::false_type{});
     }
   }
 }
