@@ -28,6 +28,7 @@
 // skipped at once, so a batch of short query counts costs no waves of idle
 // blocks, and are zero-filled before the grid dependency wait (the split
 // kernel does not touch the output).
+#include "combine_rows.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "plan.cuh"
@@ -66,163 +67,34 @@ __device__ __forceinline__ bool live_row(const CombineParams &p, Len l, int i) {
   return l.L > 0 && l.L <= p.capacity && l.ql >= 0 && l.ql <= p.Qmax && l.ql <= l.L && i < l.ql;
 }
 
-constexpr int kRowThreads = 256;
-constexpr int kRowLanes = 16;                         // float4 lanes: 64 d per CTA
-constexpr int kRowGroups = kRowThreads / kRowLanes;   // partition groups
-
 // Static plans whose streams spread over many partitions (one sequence over
-// every SM): one CTA per (output row, 64-wide slice of d).  Every CTA of a row computes
-// the row's partition weights into shared memory (a few hundred floats);
-// the P.V partials of its slice are then summed by kRowGroups groups of
-// threads, group k taking partitions k, k + kRowGroups, ... in ascending order,
-// and the group sums are added in group order: a fixed summation order that
-// does not depend on scheduling, so repeated runs agree bit for bit.  Many
-// short independent loads per thread keep the L2 busy instead of waiting on
-// one long dependent chain.
+// every SM): one CTA per (output row, 64-wide slice of d), the unit combine
+// of combine_rows.cuh with the whole CTA.
 __global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const CombineParams p) {
   extern __shared__ __align__(16) float rsm[];
   __shared__ float red[kRowThreads / 32];
   __shared__ float4 accs[kRowGroups][kRowLanes];
-
   const int nd = p.D / 64;  // d slices per row
   const int r = blockIdx.x / nd, dsl = blockIdx.x - r * nd;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = r / p.G, g = r - i * p.G;
-  const int d0 = dsl * 64;
-  __half *out = static_cast<__half *>(p.out) + (int64_t)b * p.o_sb + (int64_t)i * p.o_si +
-                (int64_t)(h * p.G + g) * p.o_sh + d0;
-
+  const int i = r / p.G;
   // lengths are inputs of the step, not results of the split kernel: read
   // them before waiting for it
   const int L = p.seq[(int64_t)b * p.seq_sb];
   const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
   // partitions of this (sequence, KV head): slots slot0 .. slot0 + nP - 1
-  int nP = 0, slot0 = 0;
-  if (!p.dev_plan) {
-    slot0 = (b * p.Hkv + h) * p.P;
-    const int T = (p.t_from_len && L > 0 && L <= p.capacity) ? max(64, plan_t_from_len(L, p.P)) : p.T;
-    nP = (L + T - 1) / T;
-  }
-
+  const int slot0 = (b * p.Hkv + h) * p.P;
+  const int T = (p.t_from_len && L > 0 && L <= p.capacity) ? max(64, plan_t_from_len(L, p.P)) : p.T;
+  const bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql;
+  const int nP = dead ? 0 : (L + T - 1) / T;
   // wait until the split kernel's partials are complete and visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql;
-  if (blockIdx.x == 0 && h == 0 && tid == 0) {  // report invalid lengths once per sequence
+  if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {  // invalid lengths, once per sequence
     if (L < 0 || L > p.capacity) atomicOr(p.status, VAE4_STATUS_BAD_LENGTH);
     else if (ql < 0 || ql > p.Qmax || (L > 0 && ql > L)) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
   }
-  if (p.dev_plan && !dead) {
-    // the device-side plan, as the split kernel's CTA of the stream's first
-    // partition recorded it (every live row's stream has one)
-    const int2 e = p.plan_tab[b * p.Hkv + h];
-    slot0 = e.x;
-    nP = e.y;
-    if (slot0 < 0 || nP < 1 || nP > p.P || slot0 + nP > p.plan_G) {  // never: a library bug
-      if (tid == 0) atomicOr(p.status, VAE4_STATUS_PLAN);
-      dead = true;
-    }
-  }
-  if (dead) nP = 0;
-  float *wm = rsm;       // m_p, then the weight w_p
-  float *wl = rsm + p.P; // l_p
-  const int64_t pstride = (int64_t)p.rows_pad;  // rows per partition
-  const float *ml = p.ws_ml + (int64_t)slot0 * pstride * 2 + r * 2;
-  const float kNegInf = -__int_as_float(0x7f800000);
-
-  // the first kPre P.V partials of this thread's group are requested now,
-  // together with the (m, l) pairs, so both L2 round trips overlap
-  const int l4 = tid % kRowLanes, grp = tid / kRowLanes;
-  const float *o = p.ws_o + (int64_t)slot0 * pstride * p.D + (int64_t)r * p.D + d0 + 4 * l4;
-  const int64_t ostride = pstride * p.D;
-  constexpr int kPre = 10;  // covers 160 partitions
-  float4 pre[kPre];
-#pragma unroll
-  for (int k = 0; k < kPre; ++k) {
-    const int q = grp + k * kRowGroups;
-    pre[k] = q < nP ? __ldcg(reinterpret_cast<const float4 *>(o + q * ostride))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
-  // ---- pass 1: (m_p, l_p), maximum over partitions with l_p > 0
-  float mx = kNegInf;
-  bool bad = false;
-  for (int q = tid; q < nP; q += kRowThreads) {
-    const float2 v = *reinterpret_cast<const float2 *>(ml + q * pstride * 2);
-    wm[q] = v.x;
-    wl[q] = v.y;
-    if (v.y < 0.f) bad = true;  // a partition met an invalid page or timed out
-    if (v.y > 0.f) mx = fmaxf(mx, v.x);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[warp] = mx;
-  const bool any_bad = __syncthreads_or(bad);
-  float M = red[0];
-#pragma unroll
-  for (int k = 1; k < kRowThreads / 32; ++k) M = fmaxf(M, red[k]);
-  __syncthreads();
-
-  // ---- pass 2: weights w_p = 2^(m_p - M) and the total sum (fixed tree)
-  float lam = 0.f;
-  for (int q = tid; q < nP; q += kRowThreads) {
-    const float l = wl[q];
-    const float w = l > 0.f ? (wm[q] == M ? 1.f : exp2f(wm[q] - M)) : 0.f;
-    wm[q] = w;
-    lam += w * l;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, o);
-  if (lane == 0) red[warp] = lam;
-  __syncthreads();
-  float Lam = 0.f;
-#pragma unroll
-  for (int k = 0; k < kRowThreads / 32; ++k) Lam += red[k];
-
-  // ---- pass 3: sum of w_p * O_p over this slice, per group (ascending p),
-  // then over groups
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int k = 0; k < kPre; ++k) {
-    const int q = grp + k * kRowGroups;
-    if (q < nP) {
-      const float w = wm[q];
-      acc.x += w * pre[k].x;
-      acc.y += w * pre[k].y;
-      acc.z += w * pre[k].z;
-      acc.w += w * pre[k].w;
-    }
-  }
-#pragma unroll 4
-  for (int q = grp + kPre * kRowGroups; q < nP; q += kRowGroups) {
-    const float w = wm[q];
-    const float4 v = __ldcg(reinterpret_cast<const float4 *>(o + q * ostride));
-    acc.x += w * v.x;
-    acc.y += w * v.y;
-    acc.z += w * v.z;
-    acc.w += w * v.w;
-  }
-  accs[grp][l4] = acc;
-  __syncthreads();
-  if (grp != 0) return;
-  float4 s = accs[0][l4];
-#pragma unroll
-  for (int k = 1; k < kRowGroups; ++k) {
-    const float4 v = accs[k][l4];
-    s.x += v.x;
-    s.y += v.y;
-    s.z += v.z;
-    s.w += v.w;
-  }
-  uint2 res = make_uint2(0u, 0u);
-  if (!dead && !any_bad && Lam > 0.f) {
-    const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // partials hold dec(V) * 2^-8
-    const __half2 lo = __floats2half2_rn(__fdiv_rn(s.x, Lam) * beta, __fdiv_rn(s.y, Lam) * beta);
-    const __half2 hi = __floats2half2_rn(__fdiv_rn(s.z, Lam) * beta, __fdiv_rn(s.w, Lam) * beta);
-    res.x = *reinterpret_cast<const uint32_t *>(&lo);
-    res.y = *reinterpret_cast<const uint32_t *>(&hi);
-  }
-  *reinterpret_cast<uint2 *>(out + 4 * l4) = res;
+  const RowScratch sc{rsm, rsm + p.P, red, accs};
+  combine_row_unit(p, b, h, r, dsl, slot0, nP, threadIdx.x, 0, sc);
 }
 
 template <int WPU>
