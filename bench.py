@@ -88,7 +88,7 @@ def peaks():
 
 
 # the split kernel the default path launches, and the sources that define it
-SPLIT_KERNEL = "vae4::split_tc_kernel<256, 48, 1>"  # automatic plan of one sequence
+SPLIT_KERNEL = "vae4::split_tc_kernel<256, 48, 1, 0>"  # automatic plan of one sequence
 SPLIT_SOURCES = ["fp8_paged_attention_e4m3_gb300/csrc/split_tc.cuh",
                  "fp8_paged_attention_e4m3_gb300/csrc/split_tc.cu",
                  "fp8_paged_attention_e4m3_gb300/csrc/split_tc_len.cu",
