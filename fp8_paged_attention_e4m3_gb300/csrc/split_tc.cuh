@@ -17,6 +17,9 @@
 //   K decoders (4)  : thread = key; exact E4M3 -> FP16 with the hardware
 //                     converter, straight into tensor memory: the A operand
 //                     of S^T = K . Q^T (lane = key, column = pair of d).
+//                     With N = 16 rows the next tile's decode of each 64-d
+//                     group starts once this tile's score MMAs of that
+//                     group are done.
 //   V decoders (4)  : warp = 32 d of every 128-d block, all 64 keys of a
 //                     half-tile: a transposing 8-bit ldmatrix of 16 keys x
 //                     16 d gives each thread four consecutive keys of one d,
@@ -84,6 +87,10 @@ struct TcCfg {
   static constexpr int DB = D / 64 < 2 ? 2 : D / 64;  // 64-d blocks of V^T (D=64 padded)
   static constexpr int MH = DB / 2;             // 128-row M halves of V^T.P^T
   static constexpr int SC = (N + 31) / 32 * 32; // TMEM columns per accumulator
+  // 64-d groups of the TMEM K tile released one by one to the next tile's
+  // decode (N = 16 only: with more rows the softmax is as long as the K
+  // chain, and the overlap measured slower)
+  static constexpr int KFG = N <= 16 ? D / 64 : 1;
   // TMEM columns: K (128 keys x D/2), two S^T buffers, O^T, then the V^T
   // half-tile ring (lane = d of a 128-d block, 32 columns per block)
   static constexpr int KCOL = 0, SCOL = 128, OCOL = 128 + 2 * SC;
@@ -111,7 +118,7 @@ struct TcCfg {
   // mbarrier indices, derived from the ring sizes so no two roles share one
   static constexpr int B_KFULL = 0, B_KEMPTY = B_KFULL + NKR, B_VFULL = B_KEMPTY + NKR,
                        B_VEMPTY = B_VFULL + NVR, B_KREADY = B_VEMPTY + NVR,
-                       B_KFREE = B_KREADY + 1, B_VREADY = B_KFREE + 1, B_VFREE = B_VREADY + NVF,
+                       B_KFREE = B_KREADY + 1, B_VREADY = B_KFREE + KFG, B_VFREE = B_VREADY + NVF,
                        B_SFULL = B_VFREE + NVF, B_SFREE = B_SFULL + 2, B_PREADY = B_SFREE + 2,
                        B_PVDONE = B_PREADY + 1, B_DRAINQK = B_PVDONE + 1,
                        B_DRAINPV = B_DRAINQK + 1, NBARS = B_DRAINPV + 1;
@@ -566,13 +573,16 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
           break;
         tc::tc_fence_after();
         const uint32_t d = tbase + C::SCOL + (j & 1) * C::SC;
+        constexpr int MPG = D / 16 / C::KFG;  // MMAs per released group
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t bq = sQ + (ks >> 2) * (N * 128) + (ks & 3) * 32;
           tc::mma_ts(d, tbase + C::KCOL + ks * 8, tc::smem_desc(bq, 16, 1024), id_qk, ks > 0);
+          if constexpr (C::KFG > 1)
+            if ((ks + 1) % MPG == 0) tc::mma_commit(bar(kKFree + ks / MPG));
         }
         tc::mma_commit(bar(kSFull + (j & 1)));
-        tc::mma_commit(bar(kKFree));
+        if constexpr (C::KFG == 1) tc::mma_commit(bar(kKFree));
         mma_issued = true;
       }
     }
@@ -620,17 +630,28 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
       for (int j = 0; j < ntiles; ++j) {
         const int t = 2 * j + kh;
         // K -> TMEM: column c holds d = 2c (low half), 2c+1 (high half).
-        // Wait for the previous tile's score MMA first: it proves every
-        // earlier K half-tile (in particular this slot's previous use, t -
-        // NKR <= t - 2) has landed and been read, so the parity wait on the
+        // Wait for the previous tile's score MMAs (of the first released
+        // group) first: they prove every decoder warp finished that tile,
+        // hence waited for every earlier K half-tile (in particular this
+        // slot's previous use, t - NKR <= t - 2), so the parity wait on the
         // slot below cannot match an older phase when pairs share slots.
+        // Later groups are overwritten once their MMAs are done.
         const int st = t % C::NKR;
         if (j > 0 && !tc::mbar_wait(bar(kKFree), (j - 1) & 1, abort_f, LIM)) break;
         if (!tc::mbar_wait(bar(kKFull + st), (t / C::NKR) & 1, abort_f, LIM)) break;
         tc::tc_fence_after();
         const uint8_t *rawK = gKR + st * C::RSLOT;
+        bool ok = true;
 #pragma unroll
         for (int grp = 0; grp < D / 64; ++grp) {
+          if constexpr (C::KFG > 1) {
+            if (grp > 0 && j > 0) {
+              if (!(ok = tc::mbar_wait(bar(kKFree + grp * C::KFG / (D / 64)), (j - 1) & 1,
+                                       abort_f, LIM)))
+                break;
+              tc::tc_fence_after();
+            }
+          }
           uint32_t r[32];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -652,6 +673,7 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
           tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32, r0);
           tc::tmem_st16(tbase + lane_off + C::KCOL + grp * 32 + 16, r1);
         }
+        if (!ok) break;
         tc::tmem_wait_st();
         tc::tc_fence_before();
         tc::mbar_arrive(bar(kKReady));
