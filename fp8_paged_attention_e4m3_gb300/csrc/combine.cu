@@ -15,19 +15,16 @@
 // or pages were invalid get zeros.
 //
 // Work decomposition: a unit is (live row, 32-wide slice of d), taken by
-// WPU warps (one, or four when each stream has many partitions).  Lane =
-// (partition group, float4 of the slice): eight lanes read 128 contiguous
-// bytes of one partition's O, four groups per warp, 4 * WPU groups per unit;
-// group g takes partitions g, g + 4 WPU, ... in ascending order and loads
-// their (max, sum) pairs itself (its eight lanes share the address).  The
-// group sums are added by a fixed shuffle tree within a warp and, with four
-// warps, in warp order, so the summation order depends only on the
-// partition count, never on scheduling: repeated runs agree bit for bit.
-// Units are taken in a grid-stride loop over the launch's capacity
-// (B x Hkv x Qmax*G rows x D/32 slices); rows without a live query are
-// skipped at once, so a batch of short query counts costs no waves of idle
-// blocks, and are zero-filled before the grid dependency wait (the split
-// kernel does not touch the output).
+// one warp.  Lane = (partition group, float4 of the slice): eight lanes read
+// 128 contiguous bytes of one partition's O, four groups per warp; group g
+// takes partitions g, g + 4, ... in ascending order and loads their (max,
+// sum) pairs itself (its eight lanes share the address).  The group sums
+// are added by a fixed shuffle tree, so the summation order depends only on
+// the partition count, never on scheduling: repeated runs agree bit for
+// bit.  Only live units are enumerated (a prefix over the sequences' live
+// rows, computed in every block from the lengths), so the warps share them
+// evenly; rows without a live query are zero-filled before the grid
+// dependency wait (the split kernel does not touch the output).
 #include "combine_rows.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -55,11 +52,6 @@ __device__ __forceinline__ Len read_len(const CombineParams &p, int b) {
   const int L = p.seq[(int64_t)b * p.seq_sb];
   const int ql = p.seq_has_qlen ? p.seq[(int64_t)b * p.seq_sb + 1] : p.Qmax;
   return Len{L, ql};
-}
-
-// barrier of the WPU warps of one unit (named barrier 1 + unit in block)
-__device__ __forceinline__ void unit_bar(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // a row (query i) of sequence b holds a live query
@@ -97,23 +89,35 @@ __global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const Combine
   combine_row_unit(p, b, h, r, dsl, slot0, nP, threadIdx.x, 0, sc);
 }
 
-template <int WPU>
+// Sequence of live unit v: the largest b with ustart[b] <= v (sequences
+// without live units own an empty range and are passed over).
+__device__ __forceinline__ int find_seq(const int *ustart, int nb, int v) {
+  int lo = 0, hi = nb;  // ustart[lo] <= v < ustart[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (ustart[mid] <= v)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const CombineParams p) {
-  constexpr int PG = 4 * WPU;             // partition groups per unit
-  constexpr int NPL = WPU == 1 ? 8 : 10;  // partitions per lane per chunk
-  constexpr int CH = PG * NPL;            // partitions per chunk
-  constexpr int UPB = kWarps / WPU;       // units per block and pass
-  static_assert(WPU == 1 || UPB <= 15, "one named barrier per unit");
+  constexpr int PG = 4;         // partition groups per warp (eight lanes each)
+  constexpr int NPL = 8;        // partitions per lane per chunk
+  constexpr int CH = PG * NPL;  // partitions per chunk
   extern __shared__ __align__(16) int csm[];
-  __shared__ float4 xw[kWarps][8];        // four-warp units: per-warp sums
-  __shared__ float xm[kWarps], xl[kWarps];
+  __shared__ int wsum[kWarps];
   const int nb_cache = p.B <= kCacheB ? p.B : 0;
-  int2 *lens = reinterpret_cast<int2 *>(csm);           // (L, q_len) per sequence
-  int2 *tab = reinterpret_cast<int2 *>(csm) + nb_cache;  // (first slot, partitions)
+  int2 *lens = reinterpret_cast<int2 *>(csm);  // (L, q_len) per sequence
   const int ntab = (p.dev_plan && p.B * p.Hkv <= kCacheTab) ? p.B * p.Hkv : 0;
+  int2 *tab = lens + nb_cache;                          // (first slot, partitions)
+  int *ustart = reinterpret_cast<int *>(tab + ntab);    // first live unit per sequence
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = p.Qmax * p.G;  // rows per (sequence, KV head)
   const int S = p.D / 32;      // slices per row
+  const int64_t nunits = (int64_t)p.B * p.Hkv * R * S;
 
   // ---- before the grid dependency wait: inputs only.  Lengths into shared
   // memory; rows without a live query zero-filled; invalid lengths reported.
@@ -154,6 +158,53 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
       }
     }
   }
+  // Live units only, numbered sequence by sequence (KV head, row, slice
+  // within each): sequence b owns Hkv * q_len * G * S of them when its
+  // lengths are valid.  An exclusive scan over the cached lengths (four per
+  // thread) gives each sequence's first unit, so the warps share exactly
+  // the live units and none takes more than ceil(live / warps).  Without
+  // the cache (very large batches) the warps walk every unit of the
+  // launch's capacity and skip the dead ones.
+  const bool compact = nb_cache > 0 && nunits < 0x7fffffffLL;
+  if (compact) {
+    int cnt[4], sum = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int b = 4 * tid + k;
+      cnt[k] = 0;
+      if (b < nb_cache) {
+        const Len l{lens[b].x, lens[b].y};
+        if (live_row(p, l, 0)) cnt[k] = p.Hkv * l.ql * p.G * S;
+      }
+      sum += cnt[k];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < kWarps ? wsum[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += t;
+      }
+      if (lane < kWarps) wsum[lane] = w;
+    }
+    __syncthreads();
+    int base = (warp > 0 ? wsum[warp - 1] : 0) + incl - sum;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int b = 4 * tid + k;
+      if (b < nb_cache) ustart[b] = base;
+      base += cnt[k];
+    }
+    if (tid == 0) ustart[nb_cache] = wsum[kWarps - 1];
+  }
 
   // ---- wait until the split kernel's partials are complete and visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -162,47 +213,49 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
   __syncthreads();
 
   const float kNegInf = -__int_as_float(0x7f800000);
-  const int uw = warp / WPU, wi = warp % WPU;  // unit within the block, warp within the unit
-  const int g = wi * 4 + (lane >> 3), f = lane & 7;
-  const int64_t nunits = (int64_t)p.B * p.Hkv * R * S;
-  // units interleaved over the blocks (block x takes x, x + grid, ...), so
-  // every SM gets a share; the pass count is the same for all warps of a
-  // block (block barriers inside four-warp units)
-  const int64_t per_pass = (int64_t)gridDim.x * UPB;
-  for (int64_t u0 = 0; u0 < nunits; u0 += per_pass) {
-    const int64_t u = u0 + (int64_t)uw * gridDim.x + blockIdx.x;
-    bool live = u < nunits;
-    int s = 0, r = 0, h = 0, b = 0, i = 0, gg = 0;
-    Len l{0, 0};
-    if (live) {
+  const int g = lane >> 3, f = lane & 7;
+  // units interleaved over the blocks (warp w of block x takes w * grid + x,
+  // then steps by the grid's warp count), so every SM gets a share
+  const int64_t nwork = compact ? (int64_t)ustart[nb_cache] : nunits;
+  const int64_t tw = (int64_t)gridDim.x * kWarps;
+  for (int64_t x = (int64_t)warp * gridDim.x + blockIdx.x; x < nwork; x += tw) {
+    int s, r, h, b;
+    Len l;
+    if (compact) {
+      const int v = (int)x;
+      b = find_seq(ustart, nb_cache, v);
+      l = Len{lens[b].x, lens[b].y};
+      const int rl = l.ql * p.G;  // live rows of this sequence per KV head
+      const int loc = v - ustart[b];
+      s = loc % S;
+      const int rr = loc / S;
+      r = rr % rl;
+      h = rr / rl;
+    } else {
       // unit -> (b, h, row, slice); slices fastest
-      s = (int)(u % S);
-      const int64_t ur = u / S;
+      s = (int)(x % S);
+      const int64_t ur = x / S;
       r = (int)(ur % R);
       const int64_t bh = ur / R;
       h = (int)(bh % p.Hkv);
       b = (int)(bh / p.Hkv);
-      i = r / p.G;
-      gg = r - i * p.G;
       l = len_of(b);
-      live = live_row(p, l, i);
+      if (!live_row(p, l, r / p.G)) continue;  // zero-filled above (uniform per warp)
     }
-    if (WPU == 1 && !live) continue;  // zero-filled above (uniform per warp)
+    const int i = r / p.G, gg = r - i * p.G;
     // partitions of this (sequence, KV head): slots slot0 .. slot0 + nP - 1
     int slot0 = 0, nP = 0;
-    if (live) {
-      if (!p.dev_plan) {
-        slot0 = (b * p.Hkv + h) * p.P;
-        const int T = p.t_from_len ? max(64, plan_t_from_len(l.L, p.P)) : p.T;
-        nP = (l.L + T - 1) / T;
-      } else {
-        const int2 e = b * p.Hkv + h < ntab ? tab[b * p.Hkv + h] : p.plan_tab[b * p.Hkv + h];
-        slot0 = e.x;
-        nP = e.y;
-        if (slot0 < 0 || nP < 1 || nP > p.P || slot0 + nP > p.plan_G) {  // never: a library bug
-          if (lane == 0 && wi == 0) atomicOr(p.status, VAE4_STATUS_PLAN);
-          nP = 0;
-        }
+    if (!p.dev_plan) {
+      slot0 = (b * p.Hkv + h) * p.P;
+      const int T = p.t_from_len ? max(64, plan_t_from_len(l.L, p.P)) : p.T;
+      nP = (l.L + T - 1) / T;
+    } else {
+      const int2 e = b * p.Hkv + h < ntab ? tab[b * p.Hkv + h] : p.plan_tab[b * p.Hkv + h];
+      slot0 = e.x;
+      nP = e.y;
+      if (slot0 < 0 || nP < 1 || nP > p.P || slot0 + nP > p.plan_G) {  // never: a library bug
+        if (lane == 0) atomicOr(p.status, VAE4_STATUS_PLAN);
+        nP = 0;
       }
     }
     const int64_t pstride = (int64_t)p.rows_pad;  // rows per partition slot
@@ -240,13 +293,6 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
       }
 #pragma unroll
       for (int off = 8; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      if constexpr (WPU > 1) {  // the unit's warps take part in the same chunks
-        if (lane == 0) xm[warp] = mx;
-        unit_bar(1 + uw, 32 * WPU);
-#pragma unroll
-        for (int w = 0; w < WPU; ++w) mx = fmaxf(mx, xm[uw * WPU + w]);
-        unit_bar(1 + uw, 32 * WPU);
-      }
       if (mx != M) {  // this chunk raised the maximum: rescale the sums so far
         const float c = M == kNegInf ? 0.f : exp2f(M - mx);
         lam *= c;
@@ -277,31 +323,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
       acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
     }
     bad = __any_sync(0xffffffffu, bad);
-    if constexpr (WPU > 1) {  // then the unit's warps, in warp order
-      if (lane < 8) xw[warp][lane] = acc;
-      if (lane == 0) {
-        xl[warp] = lam;
-        xm[warp] = bad ? 1.f : 0.f;
-      }
-      unit_bar(1 + uw, 32 * WPU);
-      if (wi == 0 && lane < 8) {
-        acc = xw[uw * WPU][lane];
-        lam = xl[uw * WPU];
-        bad = xm[uw * WPU] != 0.f;
-#pragma unroll
-        for (int w = 1; w < WPU; ++w) {
-          const float4 a = xw[uw * WPU + w][lane];
-          acc.x += a.x;
-          acc.y += a.y;
-          acc.z += a.z;
-          acc.w += a.w;
-          lam += xl[uw * WPU + w];
-          bad |= xm[uw * WPU + w] != 0.f;
-        }
-      }
-      unit_bar(1 + uw, 32 * WPU);
-    }
-    if (live && wi == 0 && lane < 8) {
+    if (lane < 8) {
       uint2 res = make_uint2(0u, 0u);
       if (!bad && lam > 0.f) {
         const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // partials hold dec(V) * 2^-8
@@ -359,28 +381,27 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
     }
     return cudaLaunchKernelEx(&cfg, combine_rows_kernel, p);
   }
-  const int WPU = 1;
   // enough blocks for every unit of the launch's capacity, at most the
   // resident blocks of one wave (units past it: grid-stride loop)
   const int64_t units = (int64_t)p.B * p.Hkv * p.Qmax * p.G * (p.D / 32);
   const int64_t cap = p.num_sms > 0 ? p.num_sms : 148;  // one block per SM
-  const int upb = kWarps / WPU;
-  int64_t nblk = (units + upb - 1) / upb;
+  int64_t nblk = (units + kWarps - 1) / kWarps;
   nblk = nblk < 1 ? 1 : (nblk > cap ? cap : nblk);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nblk, 1, 1);
   cfg.blockDim = dim3(kCombineThreads);
   const int nb_cache = p.B <= kCacheB ? p.B : 0;
   const int ntab = (p.dev_plan && p.B * p.Hkv <= kCacheTab) ? p.B * p.Hkv : 0;
-  cfg.dynamicSmemBytes = (size_t)(nb_cache + ntab) * sizeof(int2);
+  // lengths, stream table, first live unit per sequence
+  cfg.dynamicSmemBytes = (size_t)(nb_cache + ntab) * sizeof(int2) +
+                         (size_t)(nb_cache + 1) * sizeof(int);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return WPU == 4 ? cudaLaunchKernelEx(&cfg, combine_kernel<4>, p)
-                  : cudaLaunchKernelEx(&cfg, combine_kernel<1>, p);
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
 cudaError_t launch_decode_table(uint16_t *out, bool integer_path, bool e5m2,
