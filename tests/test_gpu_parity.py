@@ -385,6 +385,32 @@ def test_device_plan_large_batches(B, Hkv, Hq, D, Qmax):
     assert vae4.read_status(ws) == 0
 
 
+@pytest.mark.parametrize("B,Hkv,Hq,Lmax", [(1500, 1, 2, 80), (2100, 1, 2, 80), (1024, 4, 8, 200)])
+def test_batches_past_the_combine_caches(B, Hkv, Hq, Lmax):
+    """Batches past the combine's shared-memory caches: 1500 and 2100
+    sequences run the static plan (more than the device plan takes), the
+    latter past the cached lengths, so the combine walks the launch's whole
+    capacity and skips dead rows; 1024 sequences x 4 KV heads run the device
+    plan with its stream table read from global memory.  Empty sequences
+    and q_len = 0 among them; every live row meets the bar, every other row
+    is zero."""
+    rng = np.random.default_rng(B + Hkv)
+    seq = rng.integers(1, Lmax, size=B)
+    ql = rng.integers(0, 3, size=B)
+    seq[::7] = 0
+    ql = np.minimum(ql, seq)
+    w = W.custom("huge", B=B, Qmax=2, Hq=Hq, Hkv=Hkv, D=64, seq_lens=seq.tolist(),
+                 q_lens=ql.tolist(), seed=97 + B)
+    ref = oracle_full(w)
+    live = np.zeros(ref.shape, bool)
+    for b in range(B):
+        live[b, :int(w.q_len[b]) if w.seq_len[b] else 0] = True
+    gpu, ws = run_gpu(w, partition_tokens=0)
+    compare(gpu, ref, live)
+    assert not gpu[~live].any()
+    assert vae4.read_status(ws) == 0
+
+
 @pytest.mark.parametrize("L", [1, 700, 5000, 12345, 20000])
 def test_single_sequence_auto_plan_below_capacity(L):
     """One sequence in a launch sized for 20000 tokens: the automatic plan
