@@ -141,7 +141,7 @@ enum : int {
 // kDevPlanMaxB sequences from byte 0, the published plan at byte kPlanSh
 constexpr int kPlanSh = 12288;
 // offsets in the small region (the mbarriers occupy its first 512 bytes)
-constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmVotes = 544, kSmM = 576,
+constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmM = 576,
               kSmPos = 832, kSmMNew = 1088, kSmBase = 1344, kSmThr = 1600,
               kSmRed = 1856;  // red: 8 warps x 32 floats, ends at 2880
 
@@ -296,7 +296,6 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sSm + 8u * (uint32_t)i; };
   volatile int *abort_f = reinterpret_cast<volatile int *>(gSm + kSmAbort);
   volatile int *bad_f = reinterpret_cast<volatile int *>(gSm + kSmBad);
-  volatile int *votes = reinterpret_cast<volatile int *>(gSm + kSmVotes);
   float *m_s = reinterpret_cast<float *>(gSm + kSmM);      // running max (log2 units)
   int *pos_s = reinterpret_cast<int *>(gSm + kSmPos);      // last visible key per row
   float *mnew_s = reinterpret_cast<float *>(gSm + kSmMNew);
@@ -802,13 +801,8 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
           exceed |= s[c] > thr_s[col0 + c];
         }
       }
-      exceed = __any_sync(0xffffffffu, exceed);
-      if (lane == 0) votes[warp] = exceed ? 1 : 0;
-      tc::named_bar(1, nsm);
-      bool any = false;
-#pragma unroll
-      for (int w = 0; w < C::NSW; ++w) any |= votes[w] != 0;
-      tc::named_bar(1, nsm);  // votes read before the next tile rewrites them
+      // did any score of the tile exceed its row's threshold (all softmax warps)
+      const bool any = tc::named_bar_or(1, nsm, exceed);
       if (any) {
         // exact tile maximum per row over the 128 keys (4 quadrant warps)
 #pragma unroll
