@@ -103,11 +103,14 @@ struct TcCfg {
   static constexpr int RSLOT = 64 * D;          // one raw K or V half-tile
   static constexpr int SMALL = 2880;
   static constexpr int LIMIT = 232448 - 1024;   // opt-in maximum minus alignment slack
-  // raw slots: whatever shared memory is left, split between the rings
-  // (NVR >= NVF keeps the V decoders' slot waits unambiguous)
+  // raw slots: half of what shared memory is left (at most 8) for K; V,
+  // consumed a chain later, gets at most 4 (NVR >= NVF keeps the V
+  // decoders' slot waits unambiguous).  At D = 256 this is 5 K and 4 V
+  // half-tiles: measured faster per step than 5 and 6 (the whole space),
+  // and than 4/5, 5/5, 4/6, 3/6, 3/5 and 4/4.
   static constexpr int NRAW = (LIMIT - QB - NPB * PB - SMALL) / RSLOT;
   static constexpr int NKR = NRAW / 2 < 8 ? NRAW / 2 : 8;
-  static constexpr int NVR = NRAW - NKR < 8 ? NRAW - NKR : 8;
+  static constexpr int NVR = NRAW - NKR < 4 ? NRAW - NKR : 4;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_P = OFF_Q + QB;
   static constexpr int OFF_KR = OFF_P + NPB * PB;
