@@ -523,6 +523,13 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
     if (p.kv_cpasync)
       n_issued = cpa_produce<D>(p, h, k0, k1, nhalf, isv, ring, bar(fullb), bar(emptyb), nslot,
                                 abort_f, LIM, bad_f, cur, nxt, lp_base, btb, lane);
+    // static plans: V, consumed a chain after K, starts ~0.6 us later (a
+    // fixed pause), so K's first tile lands sooner (long step -0.2 us)
+    if (MODE != kPlanDevice && isv && !p.kv_cpasync) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 1200) {
+      }
+    }
     for (int t = 0; t < (p.kv_cpasync ? 0 : nhalf); ++t) {
       if (u > 0 && !tc::mbar_wait(bar(emptyb + st), (u - 1) & 1, abort_f, LIM)) break;
       if (lane == 0) tc::mbar_arrive_expect_tx(bar(fullb + st), C::RSLOT);
