@@ -17,9 +17,9 @@
 //   K decoders (4)  : thread = key; exact E4M3 -> FP16 with the hardware
 //                     converter, straight into tensor memory: the A operand
 //                     of S^T = K . Q^T (lane = key, column = pair of d).
-//                     With N = 16 rows the next tile's decode of each 64-d
-//                     group starts once this tile's score MMAs of that
-//                     group are done.
+//                     With N = 16 rows the next tile's decode of each 128-d
+//                     half starts once this tile's score MMAs of that half
+//                     are done.
 //   V decoders (4)  : warp = 32 d of every 128-d block, all 64 keys of a
 //                     half-tile: a transposing 8-bit ldmatrix of 16 keys x
 //                     16 d gives each thread four consecutive keys of one d,
@@ -87,10 +87,12 @@ struct TcCfg {
   static constexpr int DB = D / 64 < 2 ? 2 : D / 64;  // 64-d blocks of V^T (D=64 padded)
   static constexpr int MH = DB / 2;             // 128-row M halves of V^T.P^T
   static constexpr int SC = (N + 31) / 32 * 32; // TMEM columns per accumulator
-  // 64-d groups of the TMEM K tile released one by one to the next tile's
-  // decode (N = 16 only: with more rows the softmax is as long as the K
-  // chain, and the overlap measured slower)
-  static constexpr int KFG = N <= 16 ? D / 64 : 1;
+  // groups of the TMEM K tile released one by one to the next tile's
+  // decode: two (128-d halves) for N = 16; with more rows the softmax and
+  // value chains are as long as the K chain, and the overlap (whose TMEM
+  // stores slow the MMA issue, and each release costs a commit) measured
+  // slower with 2 or 4 groups
+  static constexpr int KFG = (N <= 16 && D >= 128) ? 2 : 1;
   // TMEM columns: K (128 keys x D/2), two S^T buffers, O^T, then the V^T
   // half-tile ring (lane = d of a 128-d block, 32 columns per block)
   static constexpr int KCOL = 0, SCOL = 128, OCOL = 128 + 2 * SC;
