@@ -66,6 +66,9 @@ __global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const Combine
   extern __shared__ __align__(16) float rsm[];
   __shared__ float red[kRowThreads / 32];
   __shared__ float4 accs[kRowGroups][kRowLanes];
+  // the next kernel on the stream may be placed as this grid's CTAs leave
+  // (its own grid-dependency wait still waits for this grid to finish)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int nd = p.D / 64;  // d slices per row
   const int r = blockIdx.x / nd, dsl = blockIdx.x - r * nd;
   const int h = blockIdx.y, b = blockIdx.z;
@@ -115,6 +118,9 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
   int2 *tab = lens + nb_cache;                          // (first slot, partitions)
   int *ustart = reinterpret_cast<int *>(tab + ntab);    // first live unit per sequence
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the next kernel on the stream may be placed as this grid's CTAs leave
+  // (its own grid-dependency wait still waits for this grid to finish)
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int R = p.Qmax * p.G;  // rows per (sequence, KV head)
   const int S = p.D / 32;      // slices per row
   const int64_t nunits = (int64_t)p.B * p.Hkv * R * S;
@@ -208,7 +214,6 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
 
   // ---- wait until the split kernel's partials are complete and visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   for (int e = tid; e < ntab; e += kCombineThreads) tab[e] = p.plan_tab[e];
   __syncthreads();
 
