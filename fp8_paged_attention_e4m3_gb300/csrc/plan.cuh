@@ -195,6 +195,27 @@ __device__ __forceinline__ bool plan_locate(const Len &len, int B, int Hkv, int 
   return false;
 }
 
+// Row group of the plan's CTA c, CTAs numbered row group by row group:
+// row group k has one CTA per partition of the sequences that keep more
+// than k row groups busy, which the partition numbering puts first, so CTA
+// c of row group k serves partition *c (returned through c) and the live
+// CTAs are exactly the first sum_b Hkv r_b P_b.  -1 past the plan.
+template <class Len>
+__device__ __forceinline__ int plan_row_group(const Len &len, int B, int Hkv, int W, int rmax,
+                                              int *c, int lane) {
+  for (int k = 0; k < rmax; ++k) {
+    int cnt = 0;
+    for (int b = lane; b < B; b += 32) {
+      const int2 v = len(b);
+      if (v.y > k) cnt += (v.x + W - 1) / W;
+    }
+    const int np = warp_sum_i(cnt) * Hkv;
+    if (*c < np) return k;
+    *c -= np;
+  }
+  return -1;
+}
+
 // Out-of-line entry points (whole warp).  Each kernel evaluates its plan
 // once; keeping the code out of the kernel body leaves the body's code
 // layout and register allocation close to what they are without the plan.
@@ -223,11 +244,15 @@ static __device__ __noinline__ void plan_stage(const PlanIn in, int *Ls, int lan
   __syncwarp();
 }
 
-// Partition x of a split launch (CTA column x, one CTA per row group), from
-// the staged pairs, with the plan's W; p = -1 past the end of the plan.
-static __device__ __noinline__ PlanCta plan_cta(const PlanIn in, const int *Ls, int x, int lane) {
+// CTA c of a split launch (one CTA per live (partition, row group), row
+// groups in turn: plan_row_group), from the staged pairs, with the plan's
+// W; p = -1 past the end of the plan.  Lane 0 also stores the CTA's
+// partition number (its workspace slot) and row group at xr[0], xr[1]
+// (0 and 0 past the plan).
+static __device__ __noinline__ PlanCta plan_cta(const PlanIn in, const int *Ls, int cta, int lane,
+                                                volatile int *xr) {
   PlanCta c{-1, -1, -1, 0, 0};
-  int W;
+  int W, x = cta, rg = -1;
   bool ok;
   if (in.B <= 32) {  // one sequence per lane, in registers
     int2 v = make_int2(0, 0);
@@ -238,14 +263,20 @@ static __device__ __noinline__ PlanCta plan_cta(const PlanIn in, const int *Ls, 
     }
     const LenReg len{v};
     W = plan_width(len, in.B, in.Hkv, in.G, lane);
-    ok = plan_locate(len, in.B, in.Hkv, W, plan_max_row_groups(in), x, lane, &c);
+    rg = plan_row_group(len, in.B, in.Hkv, W, plan_max_row_groups(in), &x, lane);
+    ok = rg >= 0 && plan_locate(len, in.B, in.Hkv, W, plan_max_row_groups(in), x, lane, &c);
   } else {
     const LenStaged len{Ls, in.Qmax, in.capacity, in.gqa, in.N};
     W = plan_width(len, in.B, in.Hkv, in.G, lane);
-    ok = plan_locate(len, in.B, in.Hkv, W, plan_max_row_groups(in), x, lane, &c);
+    rg = plan_row_group(len, in.B, in.Hkv, W, plan_max_row_groups(in), &x, lane);
+    ok = rg >= 0 && plan_locate(len, in.B, in.Hkv, W, plan_max_row_groups(in), x, lane, &c);
   }
   if (!ok) c = PlanCta{-1, -1, -1, 0, 0};
   c.W = W;
+  if (lane == 0) {
+    xr[0] = ok ? x : 0;
+    xr[1] = ok ? rg : 0;
+  }
   return c;
 }
 

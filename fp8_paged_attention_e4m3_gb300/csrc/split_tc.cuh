@@ -146,7 +146,7 @@ enum : int {
 // kDevPlanMaxB sequences from byte 0, the published plan at byte kPlanSh
 constexpr int kPlanSh = 12288;
 // offsets in the small region (the mbarriers occupy its first 512 bytes)
-constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmM = 576,
+constexpr int kSmTslot = 512, kSmAbort = 516, kSmBad = 520, kSmCta = 544, kSmM = 576,
               kSmPos = 832, kSmMNew = 1088, kSmBase = 1344, kSmThr = 1600,
               kSmRed = 1856;  // red: 8 warps x 32 floats, ends at 2880
 
@@ -382,14 +382,18 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
     // capacity with Qmax queries (host-computed W and partitions per
     // stream), which is the plan whenever the lengths are the capacity, and
     // fetch again if not.
+    // (at the capacity every sequence keeps the same row groups, so CTA c
+    // serves partition c mod the plan's partition count)
     const int npg = p.plan_np_guess;
-    const int xs = (int)blockIdx.x / npg;  // stream of the guess
-    const int bg = xs / p.Hkv, k0g = ((int)blockIdx.x - xs * npg) * p.plan_W_guess;
+    const int xg = (int)(blockIdx.x % (unsigned)(p.B * p.Hkv * npg));
+    const int xs = xg / npg;  // stream of the guess
+    const int bg = xs / p.Hkv, k0g = (xg - xs * npg) * p.plan_W_guess;
     if (bg < p.B) fetch_bt(bg, k0g);
     // The K producer warp evaluates the plan and passes it on through the
     // P^T buffer, unused until the first tile: the (L, q_len) pairs of the
     // batch staged at its start, then b, h, p, W, L and q_len of sequence b
-    // at kPlanSh.
+    // at kPlanSh; the CTA's partition number (workspace slot) and row group
+    // go to the small region for the epilogue.
     static_assert(C::PB >= kPlanSh + 64 && 2 * 4 * kDevPlanMaxB <= kPlanSh, "plan scratch");
     int *plan_ls = reinterpret_cast<int *>(gP);
     volatile int *plan_sh = reinterpret_cast<volatile int *>(gP + kPlanSh);
@@ -397,7 +401,8 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
       const PlanIn pin{p.seq, p.seq_sb, p.seq_has_qlen, p.Qmax, p.capacity, p.B, p.Hkv,
                        p.plan_G, p.G, N};
       plan_stage(pin, plan_ls, lane);
-      const PlanCta c = plan_cta(pin, plan_ls, blockIdx.x, lane);
+      volatile int *xr = reinterpret_cast<volatile int *>(gSm + kSmCta);
+      const PlanCta c = plan_cta(pin, plan_ls, blockIdx.x, lane, xr);
       if (lane == 0) {
         plan_sh[0] = c.b;
         plan_sh[1] = c.h;
@@ -406,8 +411,7 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
         plan_sh[4] = c.p >= 0 ? plan_ls[2 * c.b] : 0;
         plan_sh[5] = c.p >= 0 ? plan_ls[2 * c.b + 1] : 0;
         // the stream's first slot and partition count, for the combine
-        if (c.p == 0 && blockIdx.y == 0)
-          p.plan_tab[c.b * p.Hkv + c.h] = make_int2((int)blockIdx.x, c.np);
+        if (c.p == 0 && xr[1] == 0) p.plan_tab[c.b * p.Hkv + c.h] = make_int2(xr[0], c.np);
       }
     }
     __syncthreads();
@@ -438,12 +442,20 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
       fetch_bt(b, part * T);
     }
   }
-  // row group and workspace slot, from the CTA index alone (cheap to
-  // recompute where they are needed, in the epilogue)
+  // row group and workspace slot: from the CTA index (static grids) or
+  // the plan's values in shared memory (device plan), cheap to fetch again
+  // where they are needed, in the epilogue
   constexpr bool DEV = MODE == kPlanDevice;
-  auto cta_rg = [&]() -> int { return DEV ? (int)blockIdx.y : (int)(blockIdx.y % a.n_rg); };
+  // (device plan: the plan's values; the shared address is recomputed from
+  // the symbol where they are read)
+  auto cta_sm = [&]() -> uint32_t {
+    return ((smem_u32(smem_raw) + 1023u) & ~1023u) + C::OFF_SMALL + kSmCta;
+  };
+  auto cta_rg = [&]() -> int {
+    return DEV ? tc::ld_shared_s32(cta_sm() + 4) : (int)(blockIdx.y % a.n_rg);
+  };
   auto cta_slot = [&]() -> int64_t {
-    return DEV ? (int64_t)blockIdx.x
+    return DEV ? (int64_t)tc::ld_shared_s32(cta_sm())
                : ((int64_t)blockIdx.z * p.Hkv + blockIdx.y / a.n_rg) * p.P + blockIdx.x;
   };
   const int row0 = cta_rg() * N;  // first row of this CTA's row group
@@ -1044,10 +1056,10 @@ cudaError_t launch_tc(const SplitParams &p, const TcArgs &a, const CUtensorMap &
   // kernel on the stream drains; the kernel waits for it before its first
   // global-memory access that depends on it
   cudaLaunchConfig_t cfg = {};
-  // device plan: (partition, row group); the plan numbers the partitions of
-  // sequences with more live row groups first, so every live CTA of the
-  // second grid row comes before the ones that leave at once
-  cfg.gridDim = MODE == kPlanDevice ? dim3(p.plan_G, a.n_rg, 1) : dim3(p.P, p.Hkv * a.n_rg, p.B);
+  // device plan: one CTA per live (partition, row group), numbered row
+  // group by row group (plan_row_group), so the live CTAs are the first
+  // ones and all start in the first wave
+  cfg.gridDim = MODE == kPlanDevice ? dim3(p.plan_G, 1, 1) : dim3(p.P, p.Hkv * a.n_rg, p.B);
   cfg.blockDim = dim3(C::NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
