@@ -537,9 +537,9 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
     if (p.kv_cpasync)
       n_issued = cpa_produce<D>(p, h, k0, k1, nhalf, isv, ring, bar(fullb), bar(emptyb), nslot,
                                 abort_f, LIM, bad_f, cur, nxt, lp_base, btb, lane);
-    // static plans: V, consumed a chain after K, starts ~0.6 us later (a
-    // fixed pause), so K's first tile lands sooner (long step -0.2 us)
-    if (MODE != kPlanDevice && isv && !p.kv_cpasync) {
+    // V, consumed a chain after K, starts ~0.6 us later (a fixed pause),
+    // so K's first tile lands sooner (long step -0.2 us, ragged split -0.4)
+    if (isv && !p.kv_cpasync) {
       const long long t0 = clock64();
       while (clock64() - t0 < 1200) {
       }
