@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const Combine
   const int T = (p.t_from_len && L > 0 && L <= p.capacity) ? max(64, plan_t_from_len(L, p.P)) : p.T;
   const bool dead = L <= 0 || L > p.capacity || ql < 0 || ql > p.Qmax || ql > L || i >= ql;
   const int nP = dead ? 0 : (L + T - 1) / T;
+  const float sv = __ldg(p.scales + h * p.scale_sh + 1);  // the head's V scale (an input)
   // wait until the split kernel's partials are complete and visible
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {  // invalid lengths, once per sequence
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_rows_kernel(const Combine
     else if (ql < 0 || ql > p.Qmax || (L > 0 && ql > L)) atomicOr(p.status, VAE4_STATUS_BAD_QLEN);
   }
   const RowScratch sc{rsm, rsm + p.P, red, accs};
-  combine_row_unit(p, b, h, r, dsl, slot0, nP, threadIdx.x, 0, sc);
+  combine_row_unit(p, b, h, r, dsl, slot0, nP, sv, threadIdx.x, 0, sc);
 }
 
 // Sequence of live unit v: the largest b with ustart[b] <= v (sequences
@@ -268,6 +269,8 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
     const float *o = p.ws_o + ((int64_t)slot0 * pstride + r) * p.D + 32 * s + 4 * f;
     const int64_t ostride = pstride * p.D;
 
+    // the head's V scale, requested with the partials (not after them)
+    const float sv = __ldg(p.scales + h * p.scale_sh + 1);
     float M = kNegInf, lam = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     bool bad = false;
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const Combi
     if (lane < 8) {
       uint2 res = make_uint2(0u, 0u);
       if (!bad && lam > 0.f) {
-        const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // partials hold dec(V) * 2^-8
+        const float beta = sv * 256.0f;  // partials hold dec(V) * 2^-8
         const __half2 lo = __floats2half2_rn(__fdiv_rn(acc.x, lam) * beta, __fdiv_rn(acc.y, lam) * beta);
         const __half2 hi = __floats2half2_rn(__fdiv_rn(acc.z, lam) * beta, __fdiv_rn(acc.w, lam) * beta);
         res.x = *reinterpret_cast<const uint32_t *>(&lo);

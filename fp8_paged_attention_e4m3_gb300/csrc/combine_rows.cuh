@@ -47,10 +47,11 @@ __device__ __forceinline__ bool row_bar_or(int id, bool v) {
 }
 
 // slot0 / nP: the unit's stream's first partition slot and partition count
-// (nP = 0 for a row without a live query: zeros).  tid in [0, 256).
+// (nP = 0 for a row without a live query: zeros); sv: the head's V scale.
+// tid in [0, 256).
 __device__ __forceinline__ void combine_row_unit(const CombineParams &p, int b, int h, int r,
-                                                 int dsl, int slot0, int nP, int tid, int bar_id,
-                                                 const RowScratch &sc) {
+                                                 int dsl, int slot0, int nP, float sv, int tid,
+                                                 int bar_id, const RowScratch &sc) {
   const int lane = tid & 31, warp = tid >> 5;
   const int i = r / p.G, g = r - i * p.G;
   const int d0 = dsl * 64;
@@ -147,7 +148,7 @@ __device__ __forceinline__ void combine_row_unit(const CombineParams &p, int b, 
     }
     uint2 res = make_uint2(0u, 0u);
     if (nP > 0 && !any_bad && Lam > 0.f) {
-      const float beta = p.scales[h * p.scale_sh + 1] * 256.0f;  // partials hold dec(V) * 2^-8
+      const float beta = sv * 256.0f;  // partials hold dec(V) * 2^-8
       const __half2 lo = __floats2half2_rn(__fdiv_rn(s.x, Lam) * beta, __fdiv_rn(s.y, Lam) * beta);
       const __half2 hi = __floats2half2_rn(__fdiv_rn(s.z, Lam) * beta, __fdiv_rn(s.w, Lam) * beta);
       res.x = *reinterpret_cast<const uint32_t *>(&lo);
