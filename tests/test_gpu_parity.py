@@ -359,11 +359,11 @@ def test_device_plan_matches_static_plans_on_ragged_batches():
 
 @pytest.mark.parametrize("B,Hkv,Hq,D,Qmax", [(5, 1, 6, 256, 8), (40, 2, 8, 128, 8),
                                               (100, 1, 6, 64, 8), (12, 1, 6, 128, 16),
-                                              (7, 2, 12, 256, 16)])
+                                              (7, 2, 12, 256, 16), (9, 1, 5, 128, 16)])
 def test_device_plan_large_batches(B, Hkv, Hq, D, Qmax):
     """Up to 100 sequences, several KV heads, empty sequences and q_len = 0
     among them, up to 16 queries (two row groups, the second busy only for
-    some sequences; lengths far below the launch capacity, so no CTA's
+    some sequences and, at 5 query heads per KV head, never full; lengths far below the launch capacity, so no CTA's
     block-table guess holds): the automatic plan meets the bar against the
     oracle and leaves the status clear."""
     rng = np.random.default_rng(B * 7 + Hkv)
