@@ -35,10 +35,12 @@ namespace vae4 {
 
 namespace {
 
-// One block of 16 warps per SM (its registers leave room for no second
-// block): the blocks are placed as the split kernel's CTAs leave their SMs,
-// and smaller blocks piled up on the first SMs to free up (half the SMs
-// took every block of the long-context step).
+// Blocks of 16 warps, two per SM (at most 64 registers: four partitions
+// per lane per chunk): the blocks are placed as the split kernel's CTAs
+// leave their SMs; smaller blocks piled up on the first SMs to free up
+// (half the SMs took every block of the long-context step), and one block
+// per SM (eight partitions per lane) left each warp more units to combine
+// one after another.
 constexpr int kCombineThreads = 512;
 constexpr int kWarps = kCombineThreads / 32;
 constexpr int kCacheB = 2048;   // lengths cached in shared memory up to this batch
@@ -107,9 +109,9 @@ __device__ __forceinline__ int find_seq(const int *ustart, int nb, int v) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kCombineThreads, 1) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(const CombineParams p) {
   constexpr int PG = 4;         // partition groups per warp (eight lanes each)
-  constexpr int NPL = 8;        // partitions per lane per chunk
+  constexpr int NPL = 4;        // partitions per lane per chunk
   constexpr int CH = PG * NPL;  // partitions per chunk
   extern __shared__ __align__(16) int csm[];
   __shared__ int wsum[kWarps];
@@ -392,7 +394,7 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
   // enough blocks for every unit of the launch's capacity, at most the
   // resident blocks of one wave (units past it: grid-stride loop)
   const int64_t units = (int64_t)p.B * p.Hkv * p.Qmax * p.G * (p.D / 32);
-  const int64_t cap = p.num_sms > 0 ? p.num_sms : 148;  // one block per SM
+  const int64_t cap = 2 * (p.num_sms > 0 ? p.num_sms : 148);  // two blocks per SM
   int64_t nblk = (units + kWarps - 1) / kWarps;
   nblk = nblk < 1 ? 1 : (nblk > cap ? cap : nblk);
   cudaLaunchConfig_t cfg = {};
