@@ -443,11 +443,10 @@ __global__ void __launch_bounds__(TcCfg<D, N, HL>::NTHREADS, 1)
     }
   }
   // row group and workspace slot: from the CTA index (static grids) or
-  // the plan's values in shared memory (device plan), cheap to fetch again
+  // the plan's values in shared memory (device plan; the address is
+  // recomputed from the symbol where they are read), cheap to fetch again
   // where they are needed, in the epilogue
   constexpr bool DEV = MODE == kPlanDevice;
-  // (device plan: the plan's values; the shared address is recomputed from
-  // the symbol where they are read)
   auto cta_sm = [&]() -> uint32_t {
     return ((smem_u32(smem_raw) + 1023u) & ~1023u) + C::OFF_SMALL + kSmCta;
   };
